@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 SGEMM library; prints one JSON line.
+
+Default workload: FP32 SGEMM M=N=K=4092 (not a tile multiple), alpha=1,
+beta=0.5, A, B, C uniform[-1,1) from seed 1 -- the configuration the headline
+metric "SGEMM TFLOP/s at 4092^3 FP32" is quoted on.  One step is one sgemm()
+call through the C ABI (validate -> choose kernel -> encode TMA descriptors ->
+launch the FFMA kernel), with the operands resident in HBM.
+
+  value        2*M*N*K*steps*world / max-over-ranks device time (TFLOP/s)
+  e2e          the same, each step also copying A, B, C host->device from
+               pinned memory and C back (all on the launch stream)
+  roofline     the FFMA kernel against the FP32 FFMA peak
+               (SMs x 128 lanes x 2 FLOP x max SM clock): "bound": "alu"
+  cpu_baseline the fp64 oracle on host cores on a bounded row sample
+  secondary    decode shapes (GB/s vs measured HBM copy bandwidth) and the
+               large shapes, on device-generated normal data
+
+`--impl reference` times the oracle itself (the reference arm).  Under
+torchrun each rank runs an independent replica (weak scaling); timing is the
+max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM TFLOP/s at 4092³ FP32 (% of FP32 peak); GB/s (% HBM) on M≤16 shapes"
+L2_BYTES = 129 * 10**6
+# Best figure the pages print for this metric and workload: cuBLAS FP32 on an
+# RTX A6000 at 4092^3, 23,249.6 GFLOP/s ("CUDA 矩阵乘法优化：从朴素 Kernel 到接近
+# cuBLAS", results table).  Another machine: context, not the target.
+PAGES_BEST_TFLOPS = 23.2496
+
+KERNEL_SOURCES = {
+    "ffma_tma": ["dense_fp32_matrix_row_gb300/csrc/ffma_tma.cu",
+                 "dense_fp32_matrix_row_gb300/csrc/common.cuh"],
+    "decode": ["dense_fp32_matrix_row_gb300/csrc/decode.cu",
+               "dense_fp32_matrix_row_gb300/csrc/common.cuh"],
+    "tf32x3": ["dense_fp32_matrix_row_gb300/csrc/tf32x3.cu",
+               "dense_fp32_matrix_row_gb300/csrc/common.cuh"],
+}
+
+
+def source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        p = os.path.join(ROOT, rel)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        d["_source"] = "measured"
+        return d
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "_source": "fallback"}
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel, {}).get(workload)
+    if not d or d.get("source_hash") != source_hash(kernel):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10], parts[5]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])),
+                "sm_max_mhz": float(max(r[2] for r in inside)),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------------ helpers
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier_max(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_oracle(M, N, K, alpha, beta, A, B, C0, budget_s: float, threads: int = 0):
+    """Time the oracle on a leading row sample sized to ~budget_s seconds.
+    Returns (flop/s, rows, seconds, threads)."""
+    import oracle
+    orc = oracle.default()
+    probe = max(1, min(M, 8))
+    t = time.perf_counter()
+    orc.sgemm(A, B, C0, alpha=alpha, beta=beta, rows=np.arange(probe), threads=threads)
+    per_row = (time.perf_counter() - t) / probe
+    rows = int(max(1, min(M, budget_s / max(per_row, 1e-9))))
+    t = time.perf_counter()
+    orc.sgemm(A, B, C0, alpha=alpha, beta=beta, rows=np.arange(rows), threads=threads)
+    dt = time.perf_counter() - t
+    return 2.0 * rows * N * K / dt, rows, dt, (threads or orc.max_threads())
+
+
+def workload_config(name, w, extra=None):
+    cfg = {"workload": f"{name}: FP32 SGEMM M={w['M']} N={w['N']} K={w['K']} row-major, "
+                       f"alpha={w['alpha']} beta={w['beta']}, seed {w['seed']}",
+           "M": w["M"], "N": w["N"], "K": w["K"], "alpha": w["alpha"], "beta": w["beta"]}
+    cfg.update(extra or {})
+    return cfg
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import synth
+    name = args.workload
+    A, B, C0, w = synth.workload_inputs(name)
+    M, N, K = w["M"], w["N"], w["K"]
+    import oracle
+    orc = oracle.default()
+    # Size each step so the whole run stays near args.ref_budget seconds.
+    probe = max(1, min(M, 4))
+    t = time.perf_counter()
+    orc.sgemm(A, B, C0, alpha=w["alpha"], beta=w["beta"], rows=np.arange(probe))
+    per_row = (time.perf_counter() - t) / probe
+    steps_total = args.steps + args.warmup
+    rows = int(max(1, min(M, args.ref_budget / steps_total / max(per_row, 1e-9))))
+    sel = [np.arange(s * rows, s * rows + rows) % M for s in range(steps_total)]
+    for s in range(args.warmup):
+        orc.sgemm(A, B, C0, alpha=w["alpha"], beta=w["beta"], rows=sel[s])
+    t0 = time.perf_counter()
+    for s in range(args.warmup, steps_total):
+        orc.sgemm(A, B, C0, alpha=w["alpha"], beta=w["beta"], rows=sel[s])
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * N * K * args.steps
+    value = flops / dt / 1e12
+    sample = (f"{rows} of {M} rows of C per step ({rows * N * K * 2 / 1e9:.2f} GFLOP), "
+              f"{args.steps} timed steps after {args.warmup} warm-up")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(name, w, {"parallelism": "host cores, OpenMP over rows"}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": orc.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def timed_steps(fn, steps, stream):
+    """Run fn() `steps` times on `stream`, each bracketed by CUDA events.
+    Returns (total ms first-start..last-end, mean per-launch ms)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for s, e in evs:
+        s.record(stream)
+        fn()
+        e.record(stream)
+    torch.cuda.synchronize()
+    total = evs[0][0].elapsed_time(evs[-1][1])
+    per = float(np.mean([s.elapsed_time(e) for s, e in evs]))
+    return total, per
+
+
+def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3):
+    """Device-timed secondary shapes on device-generated data (timing only;
+    parity for these shapes is covered by the test suite)."""
+    out = {}
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+
+    def bench_shape(M, N, K, sigma_b, tensor_cores=False):
+        A = torch.randn((M, K), device=dev, generator=g)
+        B = torch.randn((K, N), device=dev, generator=g) * sigma_b
+        C = torch.empty((M, N), device=dev)
+        fn = lambda: sg.sgemm(A, B, C, 1.0, 0.0, stream=stream, tensor_cores=tensor_cores)
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        _, per = timed_steps(fn, steps, stream)
+        st = sg.status(stream)
+        kid = sg.select_kernel(M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), N, 0.0,
+                               C.data_ptr(), N, tensor_cores)
+        del A, B, C
+        return per, st, sg.KERNEL_NAMES.get(kid, str(kid))
+
+    for M in (1, 4, 16):
+        N, K = 14336, 4096
+        per, st, kn = bench_shape(M, N, K, 0.02)
+        nbytes = 4 * (M * K + K * N + M * N)
+        gbs = nbytes / (per * 1e-3) / 1e9
+        out[f"decode_m{M}"] = {"shape": [M, N, K], "kernel": kn, "ms": per, "GB/s": gbs,
+                               "frac_hbm": gbs / peaks["hbm_gbs"], "status": st,
+                               "TFLOP/s": 2 * M * N * K / (per * 1e-3) / 1e12}
+    big = [("sgemm_8192", 8192, 8192, 8192, 1.0), ("prefill_qkv", 8192, 12288, 4096, 0.02),
+           ("prefill_up", 8192, 14336, 4096, 0.02), ("prefill_down", 8192, 4096, 14336, 0.02)]
+    for name, M, N, K, sb in big:
+        per, st, kn = bench_shape(M, N, K, sb)
+        out[name] = {"shape": [M, N, K], "kernel": kn, "ms": per, "status": st,
+                     "TFLOP/s": 2 * M * N * K / (per * 1e-3) / 1e12}
+    per, st, kn = bench_shape(8192, 8192, 8192, 1.0, tensor_cores=True)
+    out["sgemm_8192_3xtf32"] = {"shape": [8192, 8192, 8192], "kernel": kn, "ms": per,
+                                "status": st, "TFLOP/s": 2 * 8192**3 / (per * 1e-3) / 1e12}
+    return out
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import dense_fp32_matrix_row_gb300 as sg
+    import synth
+    from dense_fp32_matrix_row_gb300 import accounting as acc
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    sg.build()
+    peaks = measured_peaks()
+
+    name = args.workload
+    A, B, C0, w = synth.workload_inputs(name)
+    M, N, K, alpha, beta = w["M"], w["N"], w["K"], w["alpha"], w["beta"]
+    stream = torch.cuda.Stream(device=dev)
+    dA = torch.from_numpy(A).to(dev)
+    dB = torch.from_numpy(B).to(dev)
+    dC = torch.from_numpy(C0).to(dev) if C0 is not None else torch.empty((M, N), device=dev)
+    kid = sg.select_kernel(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta,
+                           dC.data_ptr(), N, False)
+
+    def step():
+        sg.sgemm(dA, dB, dC, alpha, beta, stream=stream)
+
+    # Parity of this exact launch configuration on sampled rows, before timing.
+    with torch.cuda.stream(stream):
+        step()
+    st = sg.status(stream)
+    if st != sg.OK:
+        raise SystemExit(f"kernel status {sg.status_string(st)}")
+    parity = None
+    if rank == 0 and not args.no_parity:
+        import oracle
+        rows = np.unique(np.r_[np.arange(0, M, 61), [M - 1]])
+        ref = oracle.sgemm(A, B, C0, alpha=alpha, beta=beta, rows=rows)
+        got = dC.cpu().numpy()[rows]
+        err = float(np.abs(got.astype(np.float64) - ref).max() / (K * np.abs(A).max() * np.abs(B).max()))
+        parity = {"rows_checked": int(rows.size), "normwise_err": err, "gate": 1e-6,
+                  "pass": bool(err <= 1e-6)}
+
+    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                          int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    if rank == 0:
+        clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        total_ms, per_launch_ms = timed_steps(step, args.steps, stream)
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if rank == 0:
+        clocks.stop()
+    st = sg.status(stream)
+    if st != sg.OK:
+        raise SystemExit(f"kernel status {sg.status_string(st)}")
+    total_ms = barrier_max(total_ms, world, dev)
+    flops = acc.gemm_flops(M, N, K)
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # End to end: pinned host buffers, H2D of A, B, C and D2H of C each step.
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = (torch.from_numpy(C0) if C0 is not None else torch.zeros((M, N))).pin_memory()
+    hOut = torch.empty((M, N)).pin_memory()
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        if beta != 0.0:
+            dC.copy_(hC, non_blocking=True)
+        sg.sgemm(dA, dB, dC, alpha, beta, stream=stream)
+        hOut.copy_(dC, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_ms, _ = timed_steps(e2e_step, e2e_steps, stream)
+    e2e_ms = barrier_max(e2e_ms, world, dev)
+    e2e_value = flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+    h2d = 4 * (M * K + K * N + (M * N if beta != 0.0 else 0))
+    d2h = 4 * M * N
+
+    sec = None
+    if rank == 0 and not args.no_secondary:
+        with torch.cuda.stream(stream):
+            sec = secondary(sg, torch, stream, dev, peaks)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    props = torch.cuda.get_device_properties(dev)
+    peak = acc.ffma_peak_tflops(props.multi_processor_count, float(peaks.get("sm_max_mhz", 2070.0)))
+    achieved = flops / (per_launch_ms * 1e-3) / 1e12
+    traffic = ncu_traffic("ffma_tma", name)
+    cpu = None
+    if not args.no_cpu_baseline:
+        fl, rows, secs, thr = time_oracle(M, N, K, alpha, beta, A, B, C0, args.cpu_budget)
+        cpu = {"value": fl / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of {M} ({rows / M:.1%} of the {name} work), "
+                         f"{secs:.1f} s of fp64 triple loops"}
+    csum = clocks.summary(t_wall0, t_wall1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGES_BEST_TFLOPS,
+        "vs_baseline_ref": "pages' cuBLAS FP32 on an RTX A6000 at 4092^3 (23.25 TFLOP/s): "
+                           "another machine, context only",
+        "dtype": "f32", "data": "synthetic",
+        "config": workload_config(name, w, {
+            "kernel": sg.KERNEL_NAMES.get(kid, str(kid)),
+            "l2": f"operands {4 * (M * K + K * N + M * N) / 1e6:.0f} MB > L2 129 MB; no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 FLOP x "
+                                    f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz ({peaks['_source']} max clock)",
+                     "kernel": "ffma_tma_kernel", "per_launch_ms": per_launch_ms},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": csum,
+        "cpu_baseline": cpu,
+        "parity": parity,
+    }
+    if csum and csum.get("sm_mhz"):
+        line["roofline"]["frac_at_sampled_clock"] = achieved / acc.ffma_peak_tflops(
+            props.multi_processor_count, csum["sm_mhz"])
+    if sec is not None:
+        line["secondary"] = sec
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sgemm_4092")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--ref-budget", type=float, default=90.0, help="seconds for --impl reference")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--print-source-hash", metavar="KERNEL")
+    args = ap.parse_args()
+    if args.print_source_hash:
+        print(source_hash(args.print_source_hash))
+        return 0
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,171 @@
+"""Row-major FP32 GEMM for GB300 (sm_103a): Python binding of ``libsgemm_gb300.so``.
+
+``C <- alpha * A @ B + beta * C`` with A M x K, B K x N, C M x N, row-major
+(the operation of "GPU GEMM 优化完全拆解（一）", section "什么是 GEMM").  Every
+step runs in the library's CUDA kernels; this module only marshals arguments
+(torch CUDA tensors or raw device pointers) into the C ABI declared in
+``include/sgemm_gb300.h``.  There is no CPU path: if the library is missing,
+calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIBRARY, build  # noqa: F401  (build is part of the public API)
+
+__all__ = ["sgemm", "sgemm_3xtf32", "sgemm_ptr", "status", "select_kernel", "force_kernel",
+           "set_wait_limit", "selftest_wait", "status_string", "version", "SgemmError", "lib"]
+
+OK = 0
+ERR_BAD_DIM, ERR_BAD_LD, ERR_NULL_PTR, ERR_ALIAS = -1, -2, -3, -4
+ERR_CUDA, ERR_DEVICE, ERR_TIMEOUT, ERR_BAD_ARG = -5, -6, -7, -8
+
+KERNEL_AUTO, KERNEL_NONE, KERNEL_SCALE_C, KERNEL_FFMA_TMA = 0, 1, 2, 3
+KERNEL_FFMA_GENERIC, KERNEL_DECODE, KERNEL_TF32X3 = 4, 5, 6
+KERNEL_NAMES = {KERNEL_NONE: "none", KERNEL_SCALE_C: "scale_c", KERNEL_FFMA_TMA: "ffma_tma",
+                KERNEL_FFMA_GENERIC: "ffma_generic", KERNEL_DECODE: "decode",
+                KERNEL_TF32X3: "tf32x3"}
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})" if what else
+                         f"{status_string(code)} ({code})")
+
+
+_lib = None
+_i64, _f32, _vp = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+_GEMM_ARGS = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(
+                f"CUDA library {LIBRARY} is not built; run "
+                "`python -m dense_fp32_matrix_row_gb300.build` (there is no CPU fallback)")
+        L = ctypes.CDLL(LIBRARY)
+        for name in ("sgemm", "sgemm_3xtf32"):
+            getattr(L, name).argtypes = _GEMM_ARGS
+            getattr(L, name).restype = ctypes.c_int
+        L.sgemm_select_kernel.argtypes = _GEMM_ARGS[:-1] + [ctypes.c_int]
+        L.sgemm_select_kernel.restype = ctypes.c_int
+        L.sgemm_status.argtypes = [_vp]
+        L.sgemm_status.restype = ctypes.c_int
+        L.sgemm_status_string.argtypes = [ctypes.c_int]
+        L.sgemm_status_string.restype = ctypes.c_char_p
+        L.sgemm_force_kernel.argtypes = [ctypes.c_int]
+        L.sgemm_force_kernel.restype = ctypes.c_int
+        L.sgemm_set_wait_limit.argtypes = [_i64]
+        L.sgemm_set_wait_limit.restype = _i64
+        L.sgemm_selftest_wait.argtypes = [_i64, _vp]
+        L.sgemm_selftest_wait.restype = ctypes.c_int
+        L.sgemm_version.argtypes = []
+        L.sgemm_version.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().sgemm_status_string(int(code)).decode()
+
+
+def version() -> int:
+    return int(lib().sgemm_version())
+
+
+def _stream_handle(stream, device=None) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream   # torch.cuda.Stream
+
+
+def _ld(t) -> int:
+    """Row stride of a 2-D row-major tensor view (contiguous columns required)."""
+    rows, cols = t.shape
+    if t.numel() == 0:
+        return max(cols, 1)
+    if rows == 1:   # the row stride of a single row is arbitrary in torch
+        return max(t.stride(0), cols)
+    return t.stride(0)
+
+
+def _check_operand(t, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != torch.float32 or t.dim() != 2:
+        raise TypeError(f"{name} must be a 2-D float32 tensor")
+    if t.numel() and not t.is_cuda:
+        raise TypeError(f"{name} must live on a CUDA device")
+    if t.shape[1] > 1 and t.stride(1) != 1 and t.numel():
+        raise ValueError(f"{name} must be row-major with contiguous rows (stride(1) == 1)")
+
+
+def sgemm_ptr(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0, tensor_cores=False) -> int:
+    """Raw C-ABI call on device pointers; returns the status code."""
+    fn = lib().sgemm_3xtf32 if tensor_cores else lib().sgemm
+    return int(fn(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
+
+
+def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
+          tensor_cores: bool = False) -> None:
+    """C <- alpha * A @ B + beta * C in place on torch CUDA float32 tensors.
+
+    A is (M, K), B (K, N), C (M, N); each may be a row-strided view (row
+    stride >= row length).  Enqueued on ``stream`` (default: the current torch
+    stream of C's device); returns without waiting.  ``tensor_cores`` selects
+    the 3xTF32 tcgen05 path.  Raises SgemmError on a rejected call.
+    """
+    for t, n in ((A, "A"), (B, "B"), (C, "C")):
+        _check_operand(t, n)
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    dev = C.device if C.is_cuda else None
+    rc = sgemm_ptr(M, N, K, float(alpha), A.data_ptr() or None, _ld(A), B.data_ptr() or None,
+                   _ld(B), float(beta), C.data_ptr() or None, _ld(C),
+                   _stream_handle(stream, dev), tensor_cores)
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_3xtf32" if tensor_cores else "sgemm")
+
+
+def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
+    """``sgemm`` on the 3xTF32 tensor-core path."""
+    sgemm(A, B, C, alpha, beta, stream, tensor_cores=True)
+
+
+def status(stream=None) -> int:
+    """Wait for ``stream`` and return (and clear) the device's kernel error status."""
+    return int(lib().sgemm_status(_stream_handle(stream)))
+
+
+def select_kernel(M, N, K, alpha=1.0, A=16, lda=None, B=16, ldb=None, beta=0.0, C=16, ldc=None,
+                  tensor_cores=False) -> int:
+    """Kernel id sgemm() would run (host-only).  Pointers may be plain integers."""
+    lda = K if lda is None else lda
+    ldb = N if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    return int(lib().sgemm_select_kernel(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                         1 if tensor_cores else 0))
+
+
+def force_kernel(kernel_id: int) -> int:
+    return int(lib().sgemm_force_kernel(kernel_id))
+
+
+def set_wait_limit(ns: int) -> int:
+    return int(lib().sgemm_set_wait_limit(int(ns)))
+
+
+def selftest_wait(ns: int, stream=None) -> int:
+    return int(lib().sgemm_selftest_wait(int(ns), _stream_handle(stream)))

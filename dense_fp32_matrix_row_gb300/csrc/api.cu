@@ -1,0 +1,304 @@
+// api.cu -- the C ABI declared in include/sgemm_gb300.h: argument checks,
+// quick returns, kernel choice, TMA descriptor encoding and the per-device
+// kernel error word.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "sgemm_gb300.h"
+
+using namespace sgemm_gb300;
+
+namespace {
+
+// Kernels set bits here when a bounded wait runs out; sgemm_status() reads and
+// clears it.  One word per device (a __device__ variable lives in each
+// device's copy of this module).
+__device__ unsigned g_err_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int status = SGEMM_OK;
+    unsigned *err = nullptr;
+    int sm_count = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<int> g_force{SGEMM_KERNEL_AUTO};
+std::atomic<int64_t> g_wait_ns{2000000000LL};   // 2 s
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device set-up: check the architecture, find the error word, look up
+// the driver's tensor-map encoder.  Returns a status code.
+int device_state(DeviceState **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SGEMM_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+        if (major != 10 || minor != 3) {
+            st.status = SGEMM_ERR_DEVICE;
+        } else {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return SGEMM_ERR_CUDA;
+            if (cudaMemset(p, 0, sizeof(unsigned)) != cudaSuccess) return SGEMM_ERR_CUDA;
+            if (cudaDeviceSynchronize() != cudaSuccess) return SGEMM_ERR_CUDA;
+            if (!g_encode) {
+                void *fn = nullptr;
+                cudaDriverEntryPointQueryResult q;
+                if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q) != cudaSuccess ||
+                    q != cudaDriverEntryPointSuccess || fn == nullptr)
+                    return SGEMM_ERR_CUDA;
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+            }
+            st.err = static_cast<unsigned *>(p);
+            st.sm_count = sms;
+            st.status = SGEMM_OK;
+        }
+        st.ready = true;
+    }
+    *out = &st;
+    return st.status;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Byte range [lo, hi) touched by a rows x cols matrix with row stride ld.
+void span(const void *p, int64_t rows, int64_t cols, int64_t ld, uintptr_t *lo, uintptr_t *hi) {
+    *lo = reinterpret_cast<uintptr_t>(p);
+    *hi = *lo + (uintptr_t)(((rows - 1) * ld + cols) * (int64_t)sizeof(float));
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) {
+    return a0 < b1 && b0 < a1;
+}
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;   // keeps every offset far from int64 overflow
+
+// Checks shared by every entry point; on success *kernel is the choice
+// before any forcing or tensor-core preference.
+int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+               const float *B, int64_t ldb, float beta, const float *C, int64_t ldc,
+               bool *uses_ab) {
+    (void)beta;
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_BAD_DIM;
+    *uses_ab = false;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (C == nullptr) return SGEMM_ERR_NULL_PTR;
+    if (ldc < N) return SGEMM_ERR_BAD_LD;
+    if (M > kMaxElems / ldc) return SGEMM_ERR_BAD_DIM;
+    *uses_ab = (alpha != 0.0f) && (K > 0);
+    if (!*uses_ab) return SGEMM_OK;
+    if (A == nullptr || B == nullptr) return SGEMM_ERR_NULL_PTR;
+    if (lda < K || ldb < N) return SGEMM_ERR_BAD_LD;
+    if (M > kMaxElems / lda || K > kMaxElems / ldb) return SGEMM_ERR_BAD_DIM;
+    uintptr_t c0, c1, a0, a1, b0, b1;
+    span(C, M, N, ldc, &c0, &c1);
+    span(A, M, K, lda, &a0, &a1);
+    span(B, K, N, ldb, &b0, &b1);
+    if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return SGEMM_ERR_ALIAS;
+    return SGEMM_OK;
+}
+
+bool tma_ok(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+            int64_t ldb) {
+    const int64_t lim = int64_t(1) << 31;
+    return aligned16(A) && aligned16(B) && lda % 4 == 0 && ldb % 4 == 0 && M < lim && N < lim &&
+           K < lim && (M + FfmaTmaShape::BM - 1) / FfmaTmaShape::BM <= 65535;
+}
+
+bool kernel_can_run(int id, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                    const float *B, int64_t ldb) {
+    switch (id) {
+        case SGEMM_KERNEL_FFMA_TMA: return tma_ok(M, N, K, A, lda, B, ldb);
+        case SGEMM_KERNEL_FFMA_GENERIC: return (M + 63) / 64 <= 65535;
+        case SGEMM_KERNEL_DECODE: return M <= 16 && (N + 127) / 128 <= 65535;
+        default: return false;
+    }
+}
+
+int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+           const float *B, int64_t ldb, float beta, const float *C, int64_t ldc, bool tensor) {
+    bool uses_ab = false;
+    const int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &uses_ab);
+    if (rc != SGEMM_OK) return rc;
+    if (M == 0 || N == 0) return SGEMM_KERNEL_NONE;
+    if (!uses_ab) return SGEMM_KERNEL_SCALE_C;
+    const int forced = g_force.load();
+    if (forced != SGEMM_KERNEL_AUTO && kernel_can_run(forced, M, N, K, A, lda, B, ldb))
+        return forced;
+    (void)tensor;   // the tensor-core kernel is chosen here once it exists
+    if (M <= 16 && kernel_can_run(SGEMM_KERNEL_DECODE, M, N, K, A, lda, B, ldb))
+        return SGEMM_KERNEL_DECODE;
+    if (tma_ok(M, N, K, A, lda, B, ldb)) return SGEMM_KERNEL_FFMA_TMA;
+    if (kernel_can_run(SGEMM_KERNEL_FFMA_GENERIC, M, N, K, A, lda, B, ldb))
+        return SGEMM_KERNEL_FFMA_GENERIC;
+    return SGEMM_ERR_BAD_DIM;
+}
+
+// 2-D fp32 tensor map: `inner` contiguous elements per row, `rows` rows,
+// row stride `ld` elements, box of box_inner x box_rows.
+int encode_2d(CUtensorMap *map, const float *base, int64_t inner, int64_t rows, int64_t ld,
+              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda, const float *B,
+        int64_t ldb, float beta, float *C, int64_t ldc, void *stream, bool tensor) {
+    const int kid = choose(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tensor);
+    if (kid < 0) return kid;
+    if (kid == SGEMM_KERNEL_NONE) return SGEMM_OK;
+    DeviceState *st = nullptr;
+    const int ds = device_state(&st);
+    if (ds != SGEMM_OK) return ds;
+
+    GemmArgs g;
+    g.M = M; g.N = N; g.K = K;
+    g.alpha = alpha; g.beta = beta;
+    g.A = A; g.lda = lda; g.B = B; g.ldb = ldb; g.C = C; g.ldc = ldc;
+    g.stream = static_cast<cudaStream_t>(stream);
+    g.err = st->err;
+    g.wait_ns = (uint64_t)g_wait_ns.load();
+    g.sm_count = st->sm_count;
+
+    cudaError_t e = cudaSuccess;
+    switch (kid) {
+        case SGEMM_KERNEL_SCALE_C: e = launch_scale_c(g); break;
+        case SGEMM_KERNEL_FFMA_GENERIC: e = launch_ffma_generic(g); break;
+        case SGEMM_KERNEL_DECODE: e = launch_decode(g); break;
+        case SGEMM_KERNEL_FFMA_TMA: {
+            alignas(64) CUtensorMap tmA, tmB;
+            if (encode_2d(&tmA, A, K, M, lda, FfmaTmaShape::BK, FfmaTmaShape::BM,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != SGEMM_OK ||
+                encode_2d(&tmB, B, N, K, ldb, FfmaTmaShape::BN, FfmaTmaShape::BK,
+                          CU_TENSOR_MAP_SWIZZLE_NONE) != SGEMM_OK)
+                return SGEMM_ERR_CUDA;
+            e = launch_ffma_tma(g, tmA, tmB);
+            break;
+        }
+        default: return SGEMM_ERR_BAD_ARG;
+    }
+    return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+// One thread waits on a barrier that nothing completes, with the library's
+// bounded wait, and records the time-out.
+__global__ void selftest_wait_kernel(unsigned *err, uint64_t wait_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        mbar_fence_init();
+        if (!mbar_wait(smem_u32(&bar), 0, wait_ns)) record_error(err, kErrWaitTimeout);
+    }
+}
+
+}  // namespace
+
+namespace sgemm_gb300 {
+cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>(err, wait_ns);
+    return cudaGetLastError();
+}
+}  // namespace sgemm_gb300
+
+extern "C" {
+
+int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+          const float *B, int64_t ldb, float beta, float *C, int64_t ldc, void *stream) {
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, false);
+}
+
+int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                 const float *B, int64_t ldb, float beta, float *C, int64_t ldc, void *stream) {
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, true);
+}
+
+int sgemm_status(void *stream) {
+    DeviceState *st = nullptr;
+    const int ds = device_state(&st);
+    if (ds != SGEMM_OK) return ds;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SGEMM_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpy(&word, st->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
+    if (word != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(st->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return SGEMM_ERR_CUDA;
+        return SGEMM_ERR_TIMEOUT;
+    }
+    return SGEMM_OK;
+}
+
+const char *sgemm_status_string(int status) {
+    switch (status) {
+        case SGEMM_OK: return "success";
+        case SGEMM_ERR_BAD_DIM: return "invalid dimension (negative, or too large to index)";
+        case SGEMM_ERR_BAD_LD: return "leading dimension smaller than the row length";
+        case SGEMM_ERR_NULL_PTR: return "a required pointer is NULL";
+        case SGEMM_ERR_ALIAS: return "C overlaps A or B";
+        case SGEMM_ERR_CUDA: return "a CUDA runtime or driver call failed";
+        case SGEMM_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+        case SGEMM_ERR_TIMEOUT: return "a device-side bounded wait ran out";
+        case SGEMM_ERR_BAD_ARG: return "invalid argument";
+        default: return "unknown status";
+    }
+}
+
+int sgemm_select_kernel(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                        const float *B, int64_t ldb, float beta, const float *C, int64_t ldc,
+                        int tensor_cores) {
+    return choose(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tensor_cores != 0);
+}
+
+int sgemm_force_kernel(int id) {
+    if (id != SGEMM_KERNEL_AUTO && id != SGEMM_KERNEL_FFMA_TMA && id != SGEMM_KERNEL_FFMA_GENERIC &&
+        id != SGEMM_KERNEL_DECODE && id != SGEMM_KERNEL_TF32X3)
+        return SGEMM_ERR_BAD_ARG;
+    return g_force.exchange(id);
+}
+
+int64_t sgemm_set_wait_limit(int64_t ns) {
+    if (ns < 1) ns = 2000000000LL;
+    return g_wait_ns.exchange(ns);
+}
+
+int sgemm_selftest_wait(int64_t ns, void *stream) {
+    DeviceState *st = nullptr;
+    const int ds = device_state(&st);
+    if (ds != SGEMM_OK) return ds;
+    if (ns < 1) ns = 1;
+    return launch_selftest_wait(st->err, (uint64_t)ns, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? SGEMM_OK
+               : SGEMM_ERR_CUDA;
+}
+
+int sgemm_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+// common.cuh -- internal helpers shared by the sm_103a kernels of the SGEMM
+// library: launch descriptions, mbarrier and TMA wrappers (inline PTX), and
+// the bounded wait every kernel uses.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sgemm_gb300 {
+
+// Bit set in the per-device error word when a bounded wait runs out.
+constexpr unsigned kErrWaitTimeout = 1u;
+
+// Everything a kernel launcher needs besides the tensor maps.
+struct GemmArgs {
+    int64_t M, N, K;
+    float alpha, beta;
+    const float *A; int64_t lda;
+    const float *B; int64_t ldb;
+    float *C; int64_t ldc;
+    cudaStream_t stream;
+    unsigned *err;          // device pointer to the error word
+    uint64_t wait_ns;       // bounded-wait limit in nanoseconds
+    int sm_count;
+};
+
+// ---- launchers (one translation unit each) ------------------------------------
+cudaError_t launch_scale_c(const GemmArgs &g);
+cudaError_t launch_ffma_generic(const GemmArgs &g);
+cudaError_t launch_ffma_tma(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB);
+cudaError_t launch_decode(const GemmArgs &g);
+cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream);
+
+// Tile shape of the TMA FFMA kernel (the host encodes tensor-map boxes from it).
+struct FfmaTmaShape {
+    static constexpr int BM = 128, BN = 128, BK = 32;
+};
+
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make initialised barriers visible to the async (TMA) proxy and the cluster.
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait until the barrier phase with parity `parity` has completed, giving up
+// after `limit_ns` nanoseconds.  Returns false on time-out; the caller records
+// the error and leaves without touching the stage.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void record_error(unsigned *err, unsigned bits) {
+    if (err) atomicOr(err, bits);
+}
+
+// 2-D tiled TMA load of one box into shared memory, completing on `bar`.
+// x is the innermost (contiguous) coordinate, y the row coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 128-bit streaming load that does not allocate in L1 (data used once).
+__device__ __forceinline__ float4 ldg_stream_f4(const float *p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ldg_stream_f1(const float *p) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace sgemm_gb300

@@ -1,0 +1,163 @@
+/*
+ * sgemm_gb300.h -- C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * The operation is the general matrix multiply of the page "GPU GEMM 优化完全拆解
+ * （一）：从朴素 Kernel 到共享内存分块", section "什么是 GEMM":
+ *
+ *     C <- alpha * A @ B + beta * C
+ *
+ * with A an M x K matrix, B K x N and C M x N, all row-major: element (i, j)
+ * of a matrix with leading dimension ld is at ptr[i * ld + j] (the indexing of
+ * the naive kernel on "CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section
+ * "1. Kernel 1", generalised from ld = row length to any ld >= row length).
+ *
+ * Conventions shared by every entry point below
+ * -----------------------------------------------
+ * Memory      All matrix pointers are DEVICE pointers on the current CUDA
+ *             device.  The caller owns every buffer; the library never frees
+ *             or keeps a caller pointer past the call.  A and B are read-only.
+ * Stream      `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *             Every call is asynchronous with respect to the host: work is
+ *             enqueued on `stream` and the call returns without waiting.
+ * Sizes       M, N, K >= 0.  lda >= K, ldb >= N, ldc >= N whenever that
+ *             matrix is non-empty and read or written.
+ * Quick paths M == 0 or N == 0: nothing is done.  K == 0 or alpha == 0:
+ *             C <- beta * C and A, B are not read.  beta == 0: C is written
+ *             without being read, so NaN or Inf already in C does not reach
+ *             the result (the BLAS convention; the pages always read C).
+ * Aliasing    C must not overlap A or B (checked on the address ranges the
+ *             call would touch).
+ * Alignment   Any float-aligned pointer and any ld are accepted.  16-byte
+ *             aligned pointers with ld % 4 == 0 take the TMA-staged kernels;
+ *             anything else takes a slower kernel with plain loads.
+ * Accuracy    sgemm: FP32 FFMA arithmetic, each output a sum of K fp32
+ *             products accumulated in fp32 (order differs from a serial
+ *             loop).  sgemm_3xtf32: tensor-core TF32 products with the
+ *             operands split into high and low TF32 parts, FP32 accumulation.
+ *             Both are held to max|C - C_ref| / (K * max|A| * max|B|) <= 1e-6
+ *             against an fp64 reference; small-integer inputs are exact.
+ * Errors      Return values are SGEMM_* status codes (0 = success).
+ *             Argument errors are detected on the host before anything is
+ *             enqueued, and nothing is written.  Errors inside a kernel
+ *             (a bounded wait that ran out) are recorded in a per-device
+ *             word and reported by sgemm_status().
+ * Threads     Entry points may be called from several host threads at once.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define SGEMM_OK              0
+#define SGEMM_ERR_BAD_DIM    -1   /* M, N or K negative, or a size too large to index */
+#define SGEMM_ERR_BAD_LD     -2   /* lda < K, ldb < N or ldc < N for a matrix in use */
+#define SGEMM_ERR_NULL_PTR   -3   /* a pointer the call needs is NULL */
+#define SGEMM_ERR_ALIAS      -4   /* C overlaps A or B */
+#define SGEMM_ERR_CUDA       -5   /* a CUDA runtime or driver call failed */
+#define SGEMM_ERR_DEVICE     -6   /* the current device is not an sm_103 GPU */
+#define SGEMM_ERR_TIMEOUT    -7   /* a device-side bounded wait ran out (from sgemm_status) */
+#define SGEMM_ERR_BAD_ARG    -8   /* any other invalid argument */
+
+/* Kernel identifiers, for sgemm_select_kernel and sgemm_force_kernel. */
+#define SGEMM_KERNEL_AUTO          0   /* library's choice (sgemm_force_kernel only) */
+#define SGEMM_KERNEL_NONE          1   /* quick return, nothing launched */
+#define SGEMM_KERNEL_SCALE_C       2   /* C <- beta*C only (K == 0 or alpha == 0) */
+#define SGEMM_KERNEL_FFMA_TMA      3   /* TMA-staged, warp-tiled FFMA kernel */
+#define SGEMM_KERNEL_FFMA_GENERIC  4   /* plain-load tiled FFMA kernel, any alignment */
+#define SGEMM_KERNEL_DECODE        5   /* split-K streaming kernel for M <= 16 */
+#define SGEMM_KERNEL_TF32X3        6   /* 3xTF32 tensor-core kernel (sgemm_3xtf32) */
+
+/*
+ * sgemm -- C <- alpha * A @ B + beta * C in FP32 (FFMA) arithmetic.
+ *
+ *   M, N, K   matrix sizes (A: M x K, B: K x N, C: M x N), each >= 0
+ *   alpha     scale of the product
+ *   A, lda    device pointer to A and its row stride in elements
+ *   B, ldb    device pointer to B and its row stride in elements
+ *   beta      scale of the incoming C
+ *   C, ldc    device pointer to C (read when beta != 0, always written) and
+ *             its row stride in elements
+ *   stream    cudaStream_t to enqueue on
+ *
+ * Shapes with M <= 16 run the split-K streaming kernel (the decode regime of
+ * "GPU GEMM 优化完全拆解（一）", section "LLM 推理本质上是 GEMM 的串联"); the rest
+ * run the tiled FFMA kernel.  The result is deterministic: the same inputs
+ * give the same bits on every call.
+ * Returns SGEMM_OK, or an argument/launch error code (nothing enqueued).
+ */
+int sgemm(int64_t M, int64_t N, int64_t K, float alpha,
+          const float *A, int64_t lda, const float *B, int64_t ldb,
+          float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * sgemm_3xtf32 -- the same operation on the tcgen05 tensor cores.
+ *
+ * Each operand x is split into hi = tf32(x) and lo = tf32(x - hi); the
+ * kernel accumulates hi*hi + hi*lo + lo*hi in FP32 tensor memory, which keeps
+ * single-precision accuracy (the 3xTF32 error-compensated split of Ootomo and
+ * Yokota, 2022).  Arguments, conventions and errors are those of sgemm().
+ * Shapes the tensor-core kernel does not take (misaligned pointers or ld,
+ * M <= 16) run sgemm()'s FFMA kernels instead.
+ */
+int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha,
+                 const float *A, int64_t lda, const float *B, int64_t ldb,
+                 float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * sgemm_status -- wait for `stream`, then report and clear the current
+ * device's kernel error word.  Returns SGEMM_OK, SGEMM_ERR_TIMEOUT when a
+ * kernel's bounded wait ran out since the last call (that kernel skipped its
+ * stores and exited; C is unspecified), or SGEMM_ERR_CUDA.
+ */
+int sgemm_status(void *stream);
+
+/* Human-readable text for a status code; never NULL, static storage. */
+const char *sgemm_status_string(int status);
+
+/*
+ * sgemm_select_kernel -- which SGEMM_KERNEL_* sgemm() would run for these
+ * arguments (host-only, launches nothing, needs no GPU).  Returns a negative
+ * status code for arguments sgemm() would reject.  `tensor_cores` != 0 asks
+ * for the choice of sgemm_3xtf32() instead.
+ */
+int sgemm_select_kernel(int64_t M, int64_t N, int64_t K, float alpha,
+                        const float *A, int64_t lda, const float *B, int64_t ldb,
+                        float beta, const float *C, int64_t ldc, int tensor_cores);
+
+/*
+ * sgemm_force_kernel -- test hook: make later calls (all host threads) run
+ * kernel `id` whenever that kernel can take the arguments, instead of the
+ * library's choice.  SGEMM_KERNEL_AUTO restores the default.  Returns the
+ * previous setting, or SGEMM_ERR_BAD_ARG for an unknown id.
+ */
+int sgemm_force_kernel(int id);
+
+/*
+ * sgemm_set_wait_limit -- nanoseconds a device-side wait (a kernel waiting
+ * for its own copies or warps) may last before the kernel gives up, records
+ * SGEMM_ERR_TIMEOUT and exits (default 2e9 = 2 s; values < 1 restore it).
+ * Applies to launches made after the call.  Returns the previous limit.
+ */
+int64_t sgemm_set_wait_limit(int64_t ns);
+
+/*
+ * sgemm_selftest_wait -- launch one block on `stream` that waits, with the
+ * bounded-wait routine every kernel uses, on a barrier nothing completes,
+ * giving up after `ns` nanoseconds.  The next sgemm_status() must then report
+ * SGEMM_ERR_TIMEOUT while the context stays usable.  Returns the launch status.
+ */
+int sgemm_selftest_wait(int64_t ns, void *stream);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

@@ -121,7 +121,12 @@ def default() -> Oracle:
     """The oracle built from ``sgemm_oracle.c`` (compiled on first use)."""
     global _default
     if _default is None:
-        _default = Oracle(build())
+        try:
+            _default = Oracle(build())
+        except OSError:   # a library built for another machine: rebuild it here
+            with _lock:
+                compile_library()
+            _default = Oracle(LIBRARY)
     return _default
 
 

@@ -1,0 +1,118 @@
+"""Helpers for the GPU parity tests: padded device copies with canaries, the
+normwise error of the acceptance gate, and one checked library call."""
+
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+CANARY_BITS = np.uint32(0x7FC0DEAD)   # a quiet NaN with a recognisable payload
+GATE = 1e-6                           # max|C - C_ref| / (K * max|A| * max|B|)
+
+
+def normwise_err(C, Cref, A, B, K):
+    diff = np.abs(C.astype(np.float64) - Cref.astype(np.float64))
+    if diff.size == 0:
+        return 0.0
+    if np.isnan(diff).any():
+        return float("inf")
+    scale = K * (float(np.abs(A).max()) if A.size else 0.0) * (float(np.abs(B).max()) if B.size else 0.0)
+    d = float(diff.max())
+    return d / scale if scale > 0 else (0.0 if d == 0 else float("inf"))
+
+
+class Padded:
+    """A rows x cols matrix in a device buffer with row stride `ld`, starting
+    `offset` floats into the buffer, with `guard` canary floats before and
+    after and canaries in every gap column."""
+
+    def __init__(self, X: np.ndarray, ld: int | None = None, offset: int = 0, guard: int = 67,
+                 device="cuda"):
+        import torch
+        rows, cols = X.shape
+        self.rows, self.cols = rows, cols
+        self.ld = max(cols, 1) if ld is None else ld
+        self.start = guard + offset
+        n = self.start + rows * self.ld + guard
+        host = np.full(n, CANARY_BITS, dtype=np.uint32).view(np.float32)
+        if rows and cols:
+            host[self.start:self.start + rows * self.ld].reshape(rows, self.ld)[:, :cols] = X
+        self.template = host.copy()
+        self.buf = torch.from_numpy(host).to(device)
+        if rows and cols:
+            self.view = torch.as_strided(self.buf, (rows, cols), (self.ld, 1), self.start)
+        else:
+            self.view = torch.empty((rows, cols), dtype=torch.float32, device=device)
+
+    def host(self) -> np.ndarray:
+        return self.buf.cpu().numpy()
+
+    def matrix(self, host=None) -> np.ndarray:
+        h = self.host() if host is None else host
+        if not (self.rows and self.cols):
+            return np.zeros((self.rows, self.cols), dtype=np.float32)
+        return h[self.start:self.start + self.rows * self.ld].reshape(self.rows, self.ld)[:, :self.cols].copy()
+
+    def outside_intact(self, host=None) -> bool:
+        """Every float outside the matrix's own elements still holds its template bits."""
+        h = (self.host() if host is None else host).view(np.uint32)
+        t = self.template.view(np.uint32)
+        mask = np.ones(h.size, dtype=bool)
+        if self.rows and self.cols:
+            idx = self.start + (np.arange(self.rows)[:, None] * self.ld + np.arange(self.cols)[None, :])
+            mask[idx.reshape(-1)] = False
+        return bool(np.array_equal(h[mask], t[mask]))
+
+    def unchanged(self) -> bool:
+        return bool(np.array_equal(self.host().view(np.uint32), self.template.view(np.uint32)))
+
+
+def make_inputs(M, N, K, dist="uniform", seed=0, beta=0.0, sigma_b=None):
+    sb = 1.0 if sigma_b is None else sigma_b
+    A = synth.matrix(M, K, seed=seed, stream=0, dist=dist)
+    B = synth.matrix(K, N, seed=seed, stream=1, dist=dist, sigma=sb)
+    if beta != 0.0:
+        C0 = synth.matrix(M, N, seed=seed, stream=2, dist=dist)
+    else:
+        C0 = np.full((M, N), np.nan, dtype=np.float32)   # beta == 0 must not read C
+    return A, B, C0
+
+
+def run_checked(sg, A, B, C0, alpha, beta, *, kernel=None, lds=(None, None, None),
+                offsets=(0, 0, 0), tensor_cores=False, exact=False, rows=None):
+    """One library call on padded device copies; checks the status, the kernel
+    the library chose, canaries around all three operands, and parity with the
+    oracle (bit-exact if `exact`, else the normwise gate).  Returns the error."""
+    M, K = A.shape
+    N = B.shape[1]
+    pa = Padded(A, lds[0], offsets[0])
+    pb = Padded(B, lds[1], offsets[1])
+    pc = Padded(C0, lds[2], offsets[2])
+    prev = sg.force_kernel(kernel) if kernel is not None else None
+    try:
+        chosen = sg.select_kernel(M, N, K, alpha, pa.view.data_ptr() or 0, pa.ld,
+                                  pb.view.data_ptr() or 0, pb.ld, beta,
+                                  pc.view.data_ptr() or 0, pc.ld, tensor_cores)
+        sg.sgemm(pa.view, pb.view, pc.view, alpha, beta, tensor_cores=tensor_cores)
+        st = sg.status()
+    finally:
+        if prev is not None:
+            sg.force_kernel(sg.KERNEL_AUTO)
+    assert st == sg.OK, f"kernel status {st}: {sg.status_string(st)}"
+    h = pc.host()
+    C = pc.matrix(h)
+    assert pc.outside_intact(h), "a write landed outside C's elements (gap or guard)"
+    assert pa.unchanged() and pb.unchanged(), "A or B was modified"
+    use_ab = alpha != 0.0 and K > 0
+    Cref = oracle.sgemm(A, B, C0 if beta != 0.0 else None, alpha=alpha, beta=beta, rows=rows)
+    got = C if rows is None else C[rows]
+    if exact or not use_ab:
+        assert np.array_equal(got.view(np.uint32), Cref.view(np.uint32)) or np.array_equal(got, Cref), \
+            f"not bit-exact: max |diff| = {np.nanmax(np.abs(got - Cref)) if got.size else 0}"
+        err = 0.0
+    else:
+        err = normwise_err(got, Cref, A, B, K)
+        assert err <= GATE, f"normwise error {err:.3e} above {GATE}"
+    return err, chosen

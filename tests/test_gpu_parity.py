@@ -1,0 +1,250 @@
+"""Parity of the CUDA library with the fp64 oracle, through the C ABI.
+
+Every case runs on padded device buffers with NaN canaries in the gaps and
+guards (see gpu_util.Padded) and checks: the kernel the library chose, the
+status word, that nothing outside C's elements changed, and the oracle gate
+max|C - C_ref| / (K * max|A| * max|B|) <= 1e-6, or bit-exact equality on
+small-integer inputs and on the closed forms.
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import GATE, make_inputs, run_checked
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import dense_fp32_matrix_row_gb300 as sg  # noqa: E402
+
+TMA, GEN, DEC = sg.KERNEL_FFMA_TMA, sg.KERNEL_FFMA_GENERIC, sg.KERNEL_DECODE
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    sg.build()
+    sg.force_kernel(sg.KERNEL_AUTO)
+    yield
+
+
+def kernels_for(M):
+    return [TMA, GEN] + ([DEC] if M <= 16 else [])
+
+
+# ---------------------------------------------------------------- brute force grid
+GRID = [1, 5, 16, 17, 33, 128, 129]
+
+
+@pytest.mark.parametrize("M,N,K", list(itertools.product(GRID, GRID, GRID)))
+def test_grid_all_kernels(M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "uniform", seed=M * 1000 + N * 10 + K, beta=0.75)
+    for k in kernels_for(M):
+        _, chosen = run_checked(sg, A, B, C0, 1.25, 0.75, kernel=k)
+        assert chosen == k
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 260, 100), (129, 385, 77), (257, 129, 1000),
+                                   (511, 513, 31), (640, 384, 4097), (1, 2000, 3000)])
+def test_multi_tile_ragged(M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=M + N + K, beta=-0.5)
+    for k in kernels_for(M):
+        _, chosen = run_checked(sg, A, B, C0, 0.5, -0.5, kernel=k)
+        assert chosen == k
+
+
+DEC_M = [1, 2, 3, 4, 5, 8, 9, 16]
+DEC_N = [1, 3, 129, 1000]
+DEC_K = [1, 65, 700, 4097]
+
+
+@pytest.mark.parametrize("M,N,K", list(itertools.product(DEC_M, DEC_N, DEC_K)))
+def test_decode_shapes(M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=7 * M + N + K, beta=1.0, sigma_b=0.02)
+    _, chosen = run_checked(sg, A, B, C0, 1.0, 1.0)
+    assert chosen == DEC
+
+
+# ---------------------------------------------------------------- exactness
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (4, 14336, 4096), (300, 200, 1000),
+                                   (16, 129, 5000)])
+def test_small_integers_exact(M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "int", seed=3, beta=-2.0)
+    for k in kernels_for(M):
+        run_checked(sg, A, B, C0, 3.0, -2.0, kernel=k, exact=True)
+
+
+@pytest.mark.parametrize("k", [TMA, GEN, DEC])
+def test_identity_and_permutation_exact(k):
+    n = 16 if k == DEC else 200
+    B = synth.matrix(n, 150, seed=5, stream=1, dist="normal")
+    eye = np.eye(n, dtype=np.float32)
+    nan = np.full((n, 150), np.nan, dtype=np.float32)
+    run_checked(sg, eye, B, nan, 1.0, 0.0, kernel=k, exact=True)
+    p = np.random.default_rng(5).permutation(n)
+    P = np.zeros((n, n), dtype=np.float32)
+    P[np.arange(n), p] = 1.0
+    run_checked(sg, P, B, nan, 1.0, 0.0, kernel=k, exact=True)
+
+
+@pytest.mark.parametrize("k", [TMA, GEN, DEC])
+def test_rank1_exact(k):
+    M, N, K = (9 if k == DEC else 130), 70, 999
+    u = (np.arange(M) % 5 - 2).astype(np.float32)
+    v = (np.arange(N) % 7 - 3).astype(np.float32)
+    A = np.repeat(u[:, None], K, axis=1).astype(np.float32)
+    B = np.repeat(v[None, :], K, axis=0).astype(np.float32)
+    run_checked(sg, A, B, np.full((M, N), np.nan, np.float32), 1.0, 0.0, kernel=k, exact=True)
+
+
+# ---------------------------------------------------------------- alpha / beta
+@pytest.mark.parametrize("k", [TMA, GEN, DEC])
+def test_alpha_beta_semantics(k):
+    M = 12 if k == DEC else 70
+    N, K = 45, 33
+    A, B, C0 = make_inputs(M, N, K, "int", seed=11, beta=1.0)
+    for alpha, beta in [(1.0, 0.0), (1.0, 1.0), (1.0, 0.5), (-1.0, 2.0), (0.0, 3.0), (0.0, 0.0),
+                        (2.0, -1.0)]:
+        c = C0 if beta != 0.0 else np.full((M, N), np.nan, np.float32)
+        run_checked(sg, A, B, c, alpha, beta, kernel=k, exact=True)
+
+
+def test_k_zero_and_empty():
+    for (M, N) in [(5, 7), (300, 3)]:
+        A = np.zeros((M, 0), np.float32)
+        B = np.zeros((0, N), np.float32)
+        C0 = synth.matrix(M, N, seed=1, stream=2)
+        _, chosen = run_checked(sg, A, B, C0, 1.0, 0.25)
+        assert chosen == sg.KERNEL_SCALE_C
+        _, chosen = run_checked(sg, A, B, np.full((M, N), np.nan, np.float32), 1.0, 0.0)
+        assert chosen == sg.KERNEL_SCALE_C
+    for (M, N, K) in [(0, 5, 5), (5, 0, 5), (0, 0, 0)]:
+        A, B, C0 = make_inputs(M, N, K, beta=1.0)
+        _, chosen = run_checked(sg, A, B, C0, 1.0, 1.0)
+        assert chosen == sg.KERNEL_NONE
+
+
+def test_nan_in_inputs_propagates():
+    M, N, K = 64, 64, 64
+    A, B, _ = make_inputs(M, N, K, "uniform", seed=2)
+    A[3, 5] = np.nan
+    for k in (TMA, GEN):
+        from gpu_util import Padded
+        pa, pb = Padded(A), Padded(B)
+        pc = Padded(np.zeros((M, N), np.float32))
+        sg.force_kernel(k)
+        try:
+            sg.sgemm(pa.view, pb.view, pc.view, 1.0, 0.0)
+            assert sg.status() == sg.OK
+        finally:
+            sg.force_kernel(sg.KERNEL_AUTO)
+        C = pc.matrix()
+        assert np.isnan(C[3]).all() and np.isfinite(np.delete(C, 3, axis=0)).all()
+
+
+# ---------------------------------------------------------------- layouts
+@pytest.mark.parametrize("lds,offsets,expect", [
+    ((70, 53, 61), (0, 0, 0), GEN),        # ld % 4 != 0 everywhere
+    ((68, 52, 61), (0, 0, 0), TMA),        # A, B TMA-able, C scalar epilogue
+    ((68, 52, 56), (0, 0, 1), TMA),        # C misaligned by one float
+    ((68, 52, 56), (1, 0, 0), GEN),        # A misaligned
+    ((68, 52, 56), (0, 2, 0), GEN),        # B misaligned
+    ((64, 48, 48), (0, 0, 0), TMA),        # dense
+])
+def test_leading_dims_and_alignment(lds, offsets, expect):
+    M, N, K = 150, 48, 64
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=13, beta=0.5)
+    _, chosen = run_checked(sg, A, B, C0, 1.0, 0.5, lds=lds, offsets=offsets)
+    assert chosen == expect
+
+
+def test_decode_layouts():
+    M, N, K = 7, 300, 500
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=17, beta=0.5)
+    for lds, offsets in [((503, 301, 300), (0, 0, 0)), ((500, 304, 300), (1, 1, 1)),
+                         ((512, 304, 301), (0, 0, 3))]:
+        _, chosen = run_checked(sg, A, B, C0, 1.0, 0.5, lds=lds, offsets=offsets)
+        assert chosen == DEC
+
+
+def test_tall_and_wide_extremes():
+    for (M, N, K) in [(70000, 4, 8), (4, 70000, 8), (17, 5, 70000)]:
+        A, B, C0 = make_inputs(M, N, K, "uniform", seed=19, beta=0.0)
+        run_checked(sg, A, B, C0, 1.0, 0.0)
+
+
+# ---------------------------------------------------------------- behaviour
+def test_deterministic_and_streams():
+    M, N, K = 513, 257, 1031
+    A, B, _ = make_inputs(M, N, K, "normal", seed=23)
+    dA = torch.from_numpy(A).cuda()
+    dB = torch.from_numpy(B).cuda()
+    s = torch.cuda.Stream()
+    outs = []
+    for M_ in (M, 9):
+        for _ in range(2):
+            C = torch.empty((M_, N), device="cuda")
+            with torch.cuda.stream(s):
+                sg.sgemm(dA[:M_], dB, C, 1.0, 0.0, stream=s)
+            assert sg.status(s) == sg.OK
+            outs.append(C.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[2], outs[3])
+
+
+def test_rejected_arguments_raise():
+    A = torch.zeros((4, 4), device="cuda")
+    with pytest.raises(ValueError):
+        sg.sgemm(A, torch.zeros((5, 4), device="cuda"), torch.zeros((4, 4), device="cuda"))
+    with pytest.raises(sg.SgemmError) as e:
+        sg.sgemm(A, A, A)              # C aliases A
+    assert e.value.code == sg.ERR_ALIAS
+    with pytest.raises(TypeError):
+        sg.sgemm(A.double(), A, torch.zeros((4, 4), device="cuda"))
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    assert sg.status() == sg.OK
+    assert sg.selftest_wait(2_000_000) == sg.OK       # 2 ms on a barrier nothing completes
+    assert sg.status() == sg.ERR_TIMEOUT
+    assert sg.status() == sg.OK                       # cleared
+    A, B, C0 = make_inputs(130, 70, 90, "int", seed=29, beta=1.0)
+    run_checked(sg, A, B, C0, 1.0, 1.0, exact=True)   # the context still works
+
+
+# ---------------------------------------------------------------- full-size workloads
+def _sample_rows(M, stride=61):
+    return np.unique(np.r_[np.arange(0, M, stride), [M - 1]])
+
+
+@pytest.mark.parametrize("name", ["sgemm_128", "sgemm_128_int", "decode_m1", "decode_m4",
+                                  "decode_m16"])
+def test_workload_full(name):
+    A, B, C0, w = synth.workload_inputs(name)
+    if C0 is None:
+        C0 = np.full((w["M"], w["N"]), np.nan, np.float32)
+    run_checked(sg, A, B, C0, w["alpha"], w["beta"], exact=name.endswith("_int"))
+
+
+def test_workload_4092_full():
+    """4092^3, alpha=1, beta=0.5: every output against the oracle."""
+    A, B, C0, w = synth.workload_inputs("sgemm_4092")
+    err, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"])
+    assert chosen == TMA and err <= GATE
+
+
+def test_workload_4092_int_exact():
+    A, B, C0 = make_inputs(4092, 4092, 4092, "int", seed=1, beta=0.5)
+    run_checked(sg, A, B, C0, 1.0, 0.5, exact=True, rows=_sample_rows(4092, 31))
+
+
+@pytest.mark.parametrize("name", ["sgemm_8192", "prefill_qkv", "prefill_up", "prefill_down"])
+def test_workload_large_sampled_rows(name):
+    """Sampled rows (stride 61 < the 128-row tile, so every tile band is hit)."""
+    A, B, C0, w = synth.workload_inputs(name)
+    C0 = np.full((w["M"], w["N"]), np.nan, np.float32) if C0 is None else C0
+    run_checked(sg, A, B, C0, w["alpha"], w["beta"], rows=_sample_rows(w["M"]))
