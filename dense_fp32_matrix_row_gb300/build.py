@@ -49,16 +49,23 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
-    """Build the library unless it is newer than every source; returns its path."""
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False,
+          extra_flags: list[str] | None = None, library: str | None = None) -> str:
+    """Build the library unless it is newer than every source; returns its path.
+
+    ``extra_flags`` (e.g. -D tile settings) and ``library`` (an output path)
+    build a variant elsewhere without touching the default library.
+    """
+    out = library or LIBRARY
+    if not force and extra_flags is None and library is None and up_to_date():
         return LIBRARY
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    obj_dir = os.path.join(os.path.dirname(out), "obj")
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra = (["-Xptxas", "-v"] if ptxas_verbose else []) + list(extra_flags or [])
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -72,13 +79,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         for _, log in results:
             if log.strip():
                 print(log, file=sys.stderr)
-    tmp = LIBRARY + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIBRARY)
-    return LIBRARY
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -32,10 +32,6 @@ DeviceState g_dev[kMaxDevices];
 std::atomic<int> g_force{SGEMM_KERNEL_AUTO};
 std::atomic<int64_t> g_wait_ns{2000000000LL};   // 2 s
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
 // Per-device set-up: check the architecture, find the error word, look up
@@ -121,7 +117,7 @@ bool tma_ok(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const 
             int64_t ldb) {
     const int64_t lim = int64_t(1) << 31;
     return aligned16(A) && aligned16(B) && lda % 4 == 0 && ldb % 4 == 0 && M < lim && N < lim &&
-           K < lim && (M + FfmaTmaShape::BM - 1) / FfmaTmaShape::BM <= 65535;
+           K < lim && M <= ffma_tma_max_m();
 }
 
 bool kernel_can_run(int id, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
@@ -153,21 +149,6 @@ int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t
     return SGEMM_ERR_BAD_DIM;
 }
 
-// 2-D fp32 tensor map: `inner` contiguous elements per row, `rows` rows,
-// row stride `ld` elements, box of box_inner x box_rows.
-int encode_2d(CUtensorMap *map, const float *base, int64_t inner, int64_t rows, int64_t ld,
-              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swz) {
-    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
-    const cuuint32_t box[2] = {box_inner, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base),
-                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? SGEMM_OK : SGEMM_ERR_CUDA;
-}
-
 int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda, const float *B,
         int64_t ldb, float beta, float *C, int64_t ldc, void *stream, bool tensor) {
     const int kid = choose(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tensor);
@@ -185,26 +166,37 @@ int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t ld
     g.err = st->err;
     g.wait_ns = (uint64_t)g_wait_ns.load();
     g.sm_count = st->sm_count;
+    g.encode = g_encode;
 
     cudaError_t e = cudaSuccess;
     switch (kid) {
         case SGEMM_KERNEL_SCALE_C: e = launch_scale_c(g); break;
         case SGEMM_KERNEL_FFMA_GENERIC: e = launch_ffma_generic(g); break;
         case SGEMM_KERNEL_DECODE: e = launch_decode(g); break;
-        case SGEMM_KERNEL_FFMA_TMA: {
-            alignas(64) CUtensorMap tmA, tmB;
-            if (encode_2d(&tmA, A, K, M, lda, FfmaTmaShape::BK, FfmaTmaShape::BM,
-                          CU_TENSOR_MAP_SWIZZLE_128B) != SGEMM_OK ||
-                encode_2d(&tmB, B, N, K, ldb, FfmaTmaShape::BN, FfmaTmaShape::BK,
-                          CU_TENSOR_MAP_SWIZZLE_NONE) != SGEMM_OK)
-                return SGEMM_ERR_CUDA;
-            e = launch_ffma_tma(g, tmA, tmB);
-            break;
-        }
+        case SGEMM_KERNEL_FFMA_TMA: e = launch_ffma_tma(g); break;
         default: return SGEMM_ERR_BAD_ARG;
     }
     return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
 }
+
+}  // namespace
+
+namespace sgemm_gb300 {
+bool encode_tma_2d(EncodeTiledFn enc, CUtensorMap *map, const float *base, int64_t inner,
+                   int64_t rows, int64_t ld, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swz) {
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * sizeof(float)};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace sgemm_gb300
+
+namespace {
 
 // One thread waits on a barrier that nothing completes, with the library's
 // bounded wait, and records the time-out.

@@ -12,7 +12,13 @@ namespace sgemm_gb300 {
 // Bit set in the per-device error word when a bounded wait runs out.
 constexpr unsigned kErrWaitTimeout = 1u;
 
-// Everything a kernel launcher needs besides the tensor maps.
+// The driver's cuTensorMapEncodeTiled, looked up at run time.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Everything a kernel launcher needs.
 struct GemmArgs {
     int64_t M, N, K;
     float alpha, beta;
@@ -23,19 +29,25 @@ struct GemmArgs {
     unsigned *err;          // device pointer to the error word
     uint64_t wait_ns;       // bounded-wait limit in nanoseconds
     int sm_count;
+    EncodeTiledFn encode;   // tensor-map encoder
 };
+
+// 2-D fp32 tensor map over a row-major matrix: `inner` contiguous elements
+// per row, `rows` rows, row stride `ld` elements, box box_inner x box_rows,
+// out-of-range elements read as zero.  Returns false if the driver refuses.
+bool encode_tma_2d(EncodeTiledFn enc, CUtensorMap *map, const float *base, int64_t inner,
+                   int64_t rows, int64_t ld, uint32_t box_inner, uint32_t box_rows,
+                   CUtensorMapSwizzle swz);
 
 // ---- launchers (one translation unit each) ------------------------------------
 cudaError_t launch_scale_c(const GemmArgs &g);
 cudaError_t launch_ffma_generic(const GemmArgs &g);
-cudaError_t launch_ffma_tma(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB);
+cudaError_t launch_ffma_tma(const GemmArgs &g);
+// Largest M the TMA FFMA kernel's grid can cover.
+int64_t ffma_tma_max_m();
 cudaError_t launch_decode(const GemmArgs &g);
 cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream);
 
-// Tile shape of the TMA FFMA kernel (the host encodes tensor-map boxes from it).
-struct FfmaTmaShape {
-    static constexpr int BM = 128, BN = 128, BK = 32;
-};
 
 #ifdef __CUDACC__
 

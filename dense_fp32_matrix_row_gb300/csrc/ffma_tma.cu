@@ -5,157 +5,215 @@
 // "9. Kernel 10") with the staging its section "11" leaves as future work
 // done by the Tensor Memory Accelerator:
 //
-//  * one producer warp issues 2-D TMA copies of a BMxBK slice of A and a
-//    BKxBN slice of B into a STAGES-deep shared-memory ring; each stage has a
-//    "full" mbarrier (TMA bytes landed) and an "empty" mbarrier (all consumer
-//    warps finished reading), so copies run ahead of the arithmetic;
-//  * eight consumer warps (4 along M x 2 along N) each own a 32x64 warp tile;
-//    every lane owns an 8x8 thread tile and forms register outer products
-//    (the page's "2D blocktiling"), with 128-bit shared loads for both
-//    operands ("7. Kernel 6", vectorised access);
+//  * 2-D TMA copies of a BMxBK slice of A and a BKxBN slice of B fill a
+//    STAGES-deep shared-memory ring; each stage has a "full" mbarrier (TMA
+//    bytes landed) and an arrival counter.  There is no producer warp (a
+//    ninth warp would take a third of one sub-partition's registers): each
+//    warp bumps the stage's counter when it has read the stage, and the warp
+//    that arrives last issues the copy that refills it, STAGES k-tiles ahead;
+//  * WM x WN consumer warps each own a (4*TM) x (8*TN) warp tile; a lane
+//    (4 rows x 8 columns of lanes per warp) owns a TM x TN thread tile and
+//    forms register outer products (the page's "2D blocktiling"), with
+//    128-bit shared loads for both operands ("7. Kernel 6");
 //  * A stays K-contiguous in shared memory as it is in global memory: one
 //    128-bit load gives four consecutive k of one row, so no transpose is
 //    needed.  The TMA 128-byte swizzle (16-byte chunk index XOR row mod 8)
-//    puts the four rows a warp reads at one k in different banks, the
+//    puts the rows a warp reads at one k in different banks, the
 //    conflict-free layout the pages reach with padding or swizzling
 //    ("GPU GEMM 优化完全拆解（一）", section "两种解法：Padding 与线性化");
 //  * K tails and M/N edge tiles are zero-filled by TMA (out-of-range box
 //    elements read as 0) and the epilogue guards its stores; the epilogue
 //    applies C = alpha*acc + beta*C, reading C only when beta != 0.
+//
+// Lane (ty, tx) of warp (wm, wn) owns rows  wm*4*TM + ty + 4*i  (i < TM)
+//                              and columns wn*8*TN + tx*4 + 32*h + e  (h < TN/4, e < 4).
 #include "common.cuh"
+
+#ifndef FFMA_TM
+#define FFMA_TM 8
+#endif
+#ifndef FFMA_TN
+#define FFMA_TN 8
+#endif
+#ifndef FFMA_WM
+#define FFMA_WM 4
+#endif
+#ifndef FFMA_WN
+#define FFMA_WN 2
+#endif
+#ifndef FFMA_STAGES
+#define FFMA_STAGES 4
+#endif
+#ifndef FFMA_SNAKE
+#define FFMA_SNAKE 1
+#endif
 
 namespace sgemm_gb300 {
 namespace {
 
-constexpr int BM = FfmaTmaShape::BM, BN = FfmaTmaShape::BN, BK = FfmaTmaShape::BK;
-constexpr int STAGES = 4;
-constexpr int CONSUMER_WARPS = 8;
-constexpr int THREADS = (CONSUMER_WARPS + 1) * 32;
-constexpr int A_STAGE = BM * BK;   // floats
-constexpr int B_STAGE = BK * BN;   // floats
-constexpr uint32_t STAGE_BYTES = (A_STAGE + B_STAGE) * 4;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 2 * STAGES * sizeof(uint64_t);
 constexpr uint64_t DRAIN_NS = 1000000000ull;   // in-flight copies finish in microseconds
 
-static_assert(BK * 4 == 128, "A rows must be exactly one 128-byte swizzle span");
-static_assert((A_STAGE * 4) % 1024 == 0, "stages must keep 1024-byte alignment for the swizzle");
+template <int TM_, int TN_, int WM_, int WN_, int STAGES_>
+struct Cfg {
+    static constexpr int TM = TM_, TN = TN_, WM = WM_, WN = WN_, STAGES = STAGES_;
+    static constexpr int BM = WM * 4 * TM, BN = WN * 8 * TN, BK = 32;
+    static constexpr int CONSUMER_WARPS = WM * WN;
+    static constexpr int THREADS = CONSUMER_WARPS * 32;
+    static constexpr int A_STAGE = BM * BK;   // floats
+    static constexpr int B_STAGE = BK * BN;   // floats
+    static constexpr uint32_t STAGE_BYTES = (A_STAGE + B_STAGE) * 4;
+    static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + STAGES * 16;
+    static constexpr int B_BOX = BN > 256 ? 256 : BN;   // TMA box is at most 256 wide
+    static constexpr int B_BOXES = BN / B_BOX;
+    static_assert(TN % 4 == 0, "thread tile columns come in float4 groups");
+    static_assert(BK * 4 == 128, "A rows must be exactly one 128-byte swizzle span");
+    static_assert((A_STAGE * 4) % 1024 == 0 && (B_STAGE * 4) % 1024 == 0,
+                  "stages must keep 1024-byte alignment for the swizzle");
+    static_assert(BM <= 256 && BN % B_BOX == 0, "TMA box limits");
+    static_assert(SMEM <= 227 * 1024, "shared memory per block");
+};
+
+using Default = Cfg<FFMA_TM, FFMA_TN, FFMA_WM, FFMA_WN, FFMA_STAGES>;
 
 __device__ __forceinline__ float comp(const float4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
 ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                int M, int N, int K, float alpha, float beta, float *__restrict__ C, int64_t ldc,
+                int M, int N, int K, float alpha, float beta, float *__restrict__ Cm, int64_t ldc,
                 int c_vec4, unsigned *err, uint64_t wait_ns) {
+    constexpr int TM = C::TM, TN = C::TN, BK = C::BK, BN = C::BN, STAGES = C::STAGES;
     extern __shared__ unsigned char smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
     float *sA = reinterpret_cast<float *>(base);
-    float *sB = sA + STAGES * A_STAGE;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_STAGE);
-    uint64_t *empty = full + STAGES;
+    float *sB = sA + STAGES * C::A_STAGE;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_STAGE);
+    unsigned *arrived = reinterpret_cast<unsigned *>(full + STAGES);   // warps done with a stage
+    int *issued = reinterpret_cast<int *>(arrived + STAGES);           // k-tile last copied in
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+    const int m0 = blockIdx.y * C::BM, n0 = blockIdx.x * C::BN;
     const int ktiles = (K + BK - 1) / BK;
+
+    // Copy k-tile kt into stage kt % STAGES (one thread).
+    auto issue = [&](int kt) {
+        const int s = kt % STAGES;
+        issued[s] = kt;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+        tma_load_2d(smem_u32(sA + s * C::A_STAGE), &tmA, fb, kt * BK, m0);
+#pragma unroll
+        for (int q = 0; q < C::B_BOXES; ++q)
+            tma_load_2d(smem_u32(sB + s * C::B_STAGE + q * C::B_BOX * BK), &tmB, fb,
+                        n0 + q * C::B_BOX, kt * BK);
+    };
+    // After a failed wait: wait for every copy issued so far, so that none
+    // lands in this block's shared memory after the block has exited.
+    auto drain = [&]() {
+        for (int s = 0; s < STAGES; ++s) {
+            const int kt = *reinterpret_cast<volatile int *>(&issued[s]);
+            if (kt >= 0) mbar_wait(smem_u32(&full[s]), (kt / STAGES) & 1, DRAIN_NS);
+        }
+    };
 
     if (threadIdx.x == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), CONSUMER_WARPS);
+            arrived[s] = 0;
+            issued[s] = -1;
         }
         mbar_fence_init();
     }
     __syncthreads();
-
-    // ---------------------------------------------------------------- producer
-    if (warp == CONSUMER_WARPS) {
-        if (lane != 0) return;
+    if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        int kt = 0;
-        for (; kt < ktiles; ++kt) {
-            const int s = kt % STAGES;
-            const uint32_t use = kt / STAGES;
-            if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, wait_ns)) break;
-            const uint32_t fb = smem_u32(&full[s]);
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-            tma_load_2d(smem_u32(sA + s * A_STAGE), &tmA, fb, kt * BK, m0);
-            tma_load_2d(smem_u32(sB + s * B_STAGE), &tmB, fb, n0, kt * BK);
-        }
-        if (kt < ktiles) {
-            // The consumers stopped releasing stages.  Record it, then wait for
-            // the copies already issued so none lands after this block exits.
-            record_error(err, kErrWaitTimeout);
-            for (int q = (kt > STAGES ? kt - STAGES : 0); q < kt; ++q)
-                mbar_wait(smem_u32(&full[q % STAGES]), (q / STAGES) & 1, DRAIN_NS);
-        }
-        return;
+        for (int kt = 0; kt < STAGES && kt < ktiles; ++kt) issue(kt);
     }
 
-    // ---------------------------------------------------------------- consumers
-    const int wm = warp >> 1, wn = warp & 1;
+    // ---------------------------------------------------------------- main loop
+    const int wm = warp / C::WN, wn = warp % C::WN;
     const int ty = lane >> 3, tx = lane & 7;
-    const int rowbase = wm * 32 + ty;        // thread rows: rowbase + 4*i, i < 8
-    const int colbase = wn * 64 + tx * 4;    // thread cols: colbase + {0..3}, +32 + {0..3}
+    const int rowbase = wm * 4 * TM + ty;        // thread rows: rowbase + 4*i
+    const int colbase = wn * 8 * TN + tx * 4;    // thread cols: colbase + 32*h + e
+    // B is stored as B_BOXES boxes of [BK][B_BOX]; column c lives in box c / B_BOX.
 
-    float acc[8][8];
+    float acc[TM][TN];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
     for (int kt = 0; kt < ktiles; ++kt) {
         const int s = kt % STAGES;
         if (!mbar_wait(smem_u32(&full[s]), (kt / STAGES) & 1, wait_ns)) {
-            record_error(err, kErrWaitTimeout);
+            if (lane == 0) {
+                record_error(err, kErrWaitTimeout);
+                drain();
+            }
             return;
         }
-        const float *a_st = sA + s * A_STAGE + rowbase * BK;
-        const float *b_st = sB + s * B_STAGE + colbase;
+        const float *a_st = sA + s * C::A_STAGE + rowbase * BK;
+        const float *b_st = sB + s * C::B_STAGE;
 #pragma unroll
         for (int kc = 0; kc < BK / 4; ++kc) {
             // Row r = rowbase + 4i has (r & 7) = ty for even i and ty ^ 4 for odd i;
             // its k-chunk kc sits at 16-byte chunk kc ^ (r & 7).
             const int sw_even = (kc ^ ty) << 2;
             const int sw_odd = (kc ^ ty ^ 4) << 2;
-            float4 a[8];
+            float4 a[TM];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < TM; ++i)
                 a[i] = *reinterpret_cast<const float4 *>(a_st + i * 4 * BK +
                                                          ((i & 1) ? sw_odd : sw_even));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-                const float *brow = b_st + (kc * 4 + kk) * BN;
-                const float4 b0 = *reinterpret_cast<const float4 *>(brow);
-                const float4 b1 = *reinterpret_cast<const float4 *>(brow + 32);
+                const int k = kc * 4 + kk;
+                float4 b[TN / 4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int h = 0; h < TN / 4; ++h) {
+                    const int c = colbase + 32 * h;
+                    b[h] = *reinterpret_cast<const float4 *>(
+                        b_st + (c / C::B_BOX) * (C::B_BOX * BK) + k * C::B_BOX + (c % C::B_BOX));
+                }
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
                     const float av = comp(a[i], kk);
-                    acc[i][0] = fmaf(av, b0.x, acc[i][0]);
-                    acc[i][1] = fmaf(av, b0.y, acc[i][1]);
-                    acc[i][2] = fmaf(av, b0.z, acc[i][2]);
-                    acc[i][3] = fmaf(av, b0.w, acc[i][3]);
-                    acc[i][4] = fmaf(av, b1.x, acc[i][4]);
-                    acc[i][5] = fmaf(av, b1.y, acc[i][5]);
-                    acc[i][6] = fmaf(av, b1.z, acc[i][6]);
-                    acc[i][7] = fmaf(av, b1.w, acc[i][7]);
+                    // Odd rows walk the columns backwards, so consecutive FFMAs
+                    // share an operand across the row change.
+#pragma unroll
+                    for (int jj = 0; jj < TN; ++jj) {
+                        const int j = (FFMA_SNAKE && (i & 1)) ? TN - 1 - jj : jj;
+                        acc[i][j] = fmaf(av, comp(b[j / 4], j % 4), acc[i][j]);
+                    }
                 }
             }
         }
+        // Release the stage; the last warp to do so refills it STAGES k-tiles ahead.
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&arrived[s], 1u) == C::CONSUMER_WARPS - 1) {
+                arrived[s] = 0;
+                if (kt + STAGES < ktiles) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(kt + STAGES);
+                }
+            }
+        }
     }
 
     // ---------------------------------------------------------------- epilogue
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < TM; ++i) {
         const int gm = m0 + rowbase + 4 * i;
         if (gm >= M) continue;
-        float *crow = C + (int64_t)gm * ldc;
+        float *crow = Cm + (int64_t)gm * ldc;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < TN / 4; ++h) {
             const int gn = n0 + colbase + 32 * h;
             float v[4];
 #pragma unroll
@@ -183,21 +241,31 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 }
 
-}  // namespace
-
-cudaError_t launch_ffma_tma(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB) {
+template <class C>
+cudaError_t launch_cfg(const GemmArgs &g) {
+    alignas(64) CUtensorMap tmA, tmB;
+    if (!encode_tma_2d(g.encode, &tmA, g.A, g.K, g.M, g.lda, C::BK, C::BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, C::B_BOX, C::BK,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
     // The attribute is per device, so it is set on every launch (a host-side call).
-    cudaError_t e = cudaFuncSetAttribute(ffma_tma_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(ffma_tma_kernel<C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((g.N + BN - 1) / BN), (unsigned)((g.M + BM - 1) / BM));
+    const dim3 grid((unsigned)((g.N + C::BN - 1) / C::BN), (unsigned)((g.M + C::BM - 1) / C::BM));
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
-    ffma_tma_kernel<<<grid, THREADS, SMEM_BYTES, g.stream>>>(
+    ffma_tma_kernel<C><<<grid, C::THREADS, C::SMEM, g.stream>>>(
         tmA, tmB, (int)g.M, (int)g.N, (int)g.K, g.alpha, g.beta, g.C, g.ldc, c_vec4, g.err,
         g.wait_ns);
     return cudaGetLastError();
 }
+
+}  // namespace
+
+int64_t ffma_tma_max_m() { return (int64_t)65535 * Default::BM; }
+
+cudaError_t launch_ffma_tma(const GemmArgs &g) { return launch_cfg<Default>(g); }
 
 }  // namespace sgemm_gb300
