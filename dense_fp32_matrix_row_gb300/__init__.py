@@ -16,7 +16,7 @@ import os
 from .build import LIBRARY, build  # noqa: F401  (build is part of the public API)
 
 __all__ = ["sgemm", "sgemm_3xtf32", "sgemm_ptr", "status", "select_kernel", "force_kernel",
-           "set_wait_limit", "selftest_wait", "status_string", "version", "SgemmError", "lib"]
+           "set_wait_limit", "selftest_wait", "release_workspaces", "status_string", "version", "SgemmError", "lib"]
 
 OK = 0
 ERR_BAD_DIM, ERR_BAD_LD, ERR_NULL_PTR, ERR_ALIAS = -1, -2, -3, -4
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.sgemm_set_wait_limit.restype = _i64
         L.sgemm_selftest_wait.argtypes = [_i64, _vp]
         L.sgemm_selftest_wait.restype = ctypes.c_int
+        L.sgemm_release_workspaces.argtypes = []
+        L.sgemm_release_workspaces.restype = ctypes.c_int
         L.sgemm_version.argtypes = []
         L.sgemm_version.restype = ctypes.c_int
         _lib = L
@@ -165,6 +167,11 @@ def force_kernel(kernel_id: int) -> int:
 
 def set_wait_limit(ns: int) -> int:
     return int(lib().sgemm_set_wait_limit(int(ns)))
+
+
+def release_workspaces() -> int:
+    """Free the library's cached device workspaces (waits for their streams)."""
+    return int(lib().sgemm_release_workspaces())
 
 
 def selftest_wait(ns: int, stream=None) -> int:

@@ -1,10 +1,13 @@
 // api.cu -- the C ABI declared in include/sgemm_gb300.h: argument checks,
 // quick returns, kernel choice, TMA descriptor encoding and the per-device
 // kernel error word.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "sgemm_gb300.h"
@@ -33,6 +36,35 @@ std::atomic<int> g_force{SGEMM_KERNEL_AUTO};
 std::atomic<int64_t> g_wait_ns{2000000000LL};   // 2 s
 
 EncodeTiledFn g_encode = nullptr;
+
+// Workspace (A^T for the FFMA kernel): one buffer per (device, stream), grown
+// and freed in stream order, so calls on one stream reuse it safely and calls
+// on different streams never share it.
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, std::pair<void *, size_t>> g_ws;
+
+int workspace(size_t bytes, cudaStream_t s, float **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    auto &w = g_ws[{dev, reinterpret_cast<uintptr_t>(s)}];
+    if (w.second < bytes) {
+        const size_t grow = std::max(bytes, w.second + w.second / 2);
+        const size_t nb = (grow + (size_t(2) << 20) - 1) & ~((size_t(2) << 20) - 1);
+        if (w.first != nullptr) {
+            if (cudaFreeAsync(w.first, s) != cudaSuccess) return SGEMM_ERR_CUDA;
+            w = {nullptr, 0};
+        }
+        void *p = nullptr;
+        if (cudaMallocAsync(&p, nb, s) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_CUDA;
+        }
+        w = {p, nb};
+    }
+    *out = static_cast<float *>(w.first);
+    return SGEMM_OK;
+}
 
 // Per-device set-up: check the architecture, find the error word, look up
 // the driver's tensor-map encoder.  Returns a status code.
@@ -113,11 +145,15 @@ int check_args(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int
     return SGEMM_OK;
 }
 
+// The TMA FFMA kernel reads B in place and A through its transposed copy
+// (which the transpose kernel writes from any alignment and lda).
 bool tma_ok(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
             int64_t ldb) {
+    (void)A;
+    (void)lda;
     const int64_t lim = int64_t(1) << 31;
-    return aligned16(A) && aligned16(B) && lda % 4 == 0 && ldb % 4 == 0 && M < lim && N < lim &&
-           K < lim && M <= ffma_tma_max_m();
+    return aligned16(B) && ldb % 4 == 0 && M < lim && N < lim && K < lim &&
+           M <= ffma_tma_max_m() && (K + 31) / 32 <= 65535;
 }
 
 bool kernel_can_run(int id, int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
@@ -173,7 +209,14 @@ int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t ld
         case SGEMM_KERNEL_SCALE_C: e = launch_scale_c(g); break;
         case SGEMM_KERNEL_FFMA_GENERIC: e = launch_ffma_generic(g); break;
         case SGEMM_KERNEL_DECODE: e = launch_decode(g); break;
-        case SGEMM_KERNEL_FFMA_TMA: e = launch_ffma_tma(g); break;
+        case SGEMM_KERNEL_FFMA_TMA: {
+            float *ws = nullptr;
+            const int rc = workspace((size_t)K * (size_t)ffma_tma_at_ld(M) * sizeof(float),
+                                     g.stream, &ws);
+            if (rc != SGEMM_OK) return rc;
+            e = launch_ffma_tma(g, ws);
+            break;
+        }
         default: return SGEMM_ERR_BAD_ARG;
     }
     return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
@@ -289,6 +332,23 @@ int sgemm_selftest_wait(int64_t ns, void *stream) {
                    cudaSuccess
                ? SGEMM_OK
                : SGEMM_ERR_CUDA;
+}
+
+int sgemm_release_workspaces(void) {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    int rc = SGEMM_OK;
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return SGEMM_ERR_CUDA;
+    for (auto &kv : g_ws) {
+        if (kv.second.first == nullptr) continue;
+        cudaStream_t s = reinterpret_cast<cudaStream_t>(kv.first.second);
+        if (cudaSetDevice(kv.first.first) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess || cudaFree(kv.second.first) != cudaSuccess)
+            rc = SGEMM_ERR_CUDA;
+    }
+    g_ws.clear();
+    if (cudaSetDevice(cur) != cudaSuccess) rc = SGEMM_ERR_CUDA;
+    return rc;
 }
 
 int sgemm_version(void) { return 100; }

@@ -42,9 +42,15 @@ bool encode_tma_2d(EncodeTiledFn enc, CUtensorMap *map, const float *base, int64
 // ---- launchers (one translation unit each) ------------------------------------
 cudaError_t launch_scale_c(const GemmArgs &g);
 cudaError_t launch_ffma_generic(const GemmArgs &g);
-cudaError_t launch_ffma_tma(const GemmArgs &g);
+// FFMA kernel: transposes A into `workspace` (K rows of ffma_tma_at_ld(M)
+// floats, 16-byte aligned), then runs the TMA-staged kernel on A^T and B.
+cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace);
+int64_t ffma_tma_at_ld(int64_t M);
 // Largest M the TMA FFMA kernel's grid can cover.
 int64_t ffma_tma_max_m();
+// At[k*ldt + m] = A[m*lda + k] for m < M, k < K.
+cudaError_t launch_transpose(int64_t M, int64_t K, const float *A, int64_t lda, float *At,
+                             int64_t ldt, cudaStream_t stream);
 cudaError_t launch_decode(const GemmArgs &g);
 cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream);
 

@@ -16,6 +16,10 @@
  * Memory      All matrix pointers are DEVICE pointers on the current CUDA
  *             device.  The caller owns every buffer; the library never frees
  *             or keeps a caller pointer past the call.  A and B are read-only.
+ *             The FFMA path (M > 16) stages A through a transposed copy in a
+ *             library workspace: K x round_up(M, 4) floats per (device,
+ *             stream), grown on first need with cudaMallocAsync on `stream`
+ *             and kept for later calls (sgemm_release_workspaces frees it).
  * Stream      `stream` is a cudaStream_t (NULL = the legacy default stream).
  *             Every call is asynchronous with respect to the host: work is
  *             enqueued on `stream` and the call returns without waiting.
@@ -27,9 +31,10 @@
  *             the result (the BLAS convention; the pages always read C).
  * Aliasing    C must not overlap A or B (checked on the address ranges the
  *             call would touch).
- * Alignment   Any float-aligned pointer and any ld are accepted.  16-byte
- *             aligned pointers with ld % 4 == 0 take the TMA-staged kernels;
- *             anything else takes a slower kernel with plain loads.
+ * Alignment   Any float-aligned pointer and any ld are accepted.  When B is
+ *             16-byte aligned with ldb % 4 == 0 the TMA-staged kernel runs
+ *             (A and C may have any alignment); otherwise a slower kernel with
+ *             plain loads does.
  * Accuracy    sgemm: FP32 FFMA arithmetic, each output a sum of K fp32
  *             products accumulated in fp32 (order differs from a serial
  *             loop).  sgemm_3xtf32: tensor-core TF32 products with the
@@ -152,6 +157,16 @@ int64_t sgemm_set_wait_limit(int64_t ns);
  * SGEMM_ERR_TIMEOUT while the context stays usable.  Returns the launch status.
  */
 int sgemm_selftest_wait(int64_t ns, void *stream);
+
+/*
+ * sgemm_release_workspaces -- free the library's cached device workspaces
+ * (the transposed copy of A that the FFMA kernel stages from; one buffer per
+ * device and stream, grown with cudaMallocAsync on the call's stream).
+ * Waits for every stream that owns a workspace.  Safe to call at any time
+ * from a thread that has no sgemm call in progress; later calls allocate
+ * again as needed.  Returns SGEMM_OK or SGEMM_ERR_CUDA.
+ */
+int sgemm_release_workspaces(void);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int sgemm_version(void);

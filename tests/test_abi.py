@@ -81,10 +81,11 @@ def test_kernel_choice(L):
         assert sel(M, 14336, 4096, A=a, B=b, C=c) == sg.KERNEL_DECODE
     assert sel(17, 64, 64, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA
     assert sel(4092, 4092, 4092, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA
-    # misaligned pointer or ld % 4 != 0 -> plain-load kernel
-    assert sel(128, 128, 128, A=a + 4, B=b, C=c) == sg.KERNEL_FFMA_GENERIC
+    # B misaligned or ldb % 4 != 0 -> plain-load kernel; A may be anything
+    # (the TMA path reads A through its transposed copy)
+    assert sel(128, 128, 128, A=a + 4, B=b, C=c) == sg.KERNEL_FFMA_TMA
+    assert sel(128, 128, 127, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA       # lda = 127
     assert sel(128, 128, 128, A=a, B=b + 8, C=c) == sg.KERNEL_FFMA_GENERIC
-    assert sel(128, 128, 127, A=a, B=b, C=c) == sg.KERNEL_FFMA_GENERIC   # lda = 127
     assert sel(128, 130, 128, A=a, B=b, C=c) == sg.KERNEL_FFMA_GENERIC   # ldb = 130
     # C alignment does not matter for the choice (the epilogue adapts)
     assert sel(128, 128, 128, A=a, B=b, C=c + 4) == sg.KERNEL_FFMA_TMA
@@ -101,7 +102,7 @@ def test_force_kernel(L):
         assert sel(256, 256, 256, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA   # decode cannot take M > 16
         sg.force_kernel(sg.KERNEL_FFMA_TMA)
         assert sel(8, 256, 256, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA
-        assert sel(8, 256, 256, A=a + 4, B=b, C=c) == sg.KERNEL_DECODE  # TMA cannot take it
+        assert sel(8, 256, 256, A=a, B=b + 4, C=c) == sg.KERNEL_DECODE  # TMA cannot take it
     finally:
         sg.force_kernel(sg.KERNEL_AUTO)
 

@@ -152,8 +152,10 @@ def test_nan_in_inputs_propagates():
     ((70, 53, 61), (0, 0, 0), GEN),        # ld % 4 != 0 everywhere
     ((68, 52, 61), (0, 0, 0), TMA),        # A, B TMA-able, C scalar epilogue
     ((68, 52, 56), (0, 0, 1), TMA),        # C misaligned by one float
-    ((68, 52, 56), (1, 0, 0), GEN),        # A misaligned
+    ((68, 52, 56), (1, 0, 0), TMA),        # A misaligned: read through its transposed copy
+    ((70, 52, 56), (0, 0, 0), TMA),        # lda % 4 != 0: likewise
     ((68, 52, 56), (0, 2, 0), GEN),        # B misaligned
+    ((68, 53, 56), (0, 0, 0), GEN),        # ldb % 4 != 0
     ((64, 48, 48), (0, 0, 0), TMA),        # dense
 ])
 def test_leading_dims_and_alignment(lds, offsets, expect):
@@ -194,6 +196,14 @@ def test_deterministic_and_streams():
             assert sg.status(s) == sg.OK
             outs.append(C.cpu().numpy())
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[2], outs[3])
+
+
+def test_workspace_release_and_regrow():
+    A, B, C0 = make_inputs(300, 200, 260, "int", seed=31, beta=1.0)
+    run_checked(sg, A, B, C0, 1.0, 1.0, exact=True)
+    assert sg.release_workspaces() == sg.OK
+    A, B, C0 = make_inputs(700, 90, 1100, "int", seed=32, beta=0.0)
+    run_checked(sg, A, B, C0, 1.0, 0.0, exact=True)   # grows a fresh workspace
 
 
 def test_rejected_arguments_raise():
