@@ -259,6 +259,17 @@ cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t s
     selftest_wait_kernel<<<1, 32, 0, stream>>>(err, wait_ns);
     return cudaGetLastError();
 }
+
+int fill_device_args(GemmArgs &g) {
+    DeviceState *st = nullptr;
+    const int ds = device_state(&st);
+    if (ds != SGEMM_OK) return ds;
+    g.err = st->err;
+    g.wait_ns = (uint64_t)g_wait_ns.load();
+    g.sm_count = st->sm_count;
+    g.encode = g_encode;
+    return SGEMM_OK;
+}
 }  // namespace sgemm_gb300
 
 extern "C" {
@@ -301,6 +312,9 @@ const char *sgemm_status_string(int status) {
         case SGEMM_ERR_DEVICE: return "the current device is not an sm_103 GPU";
         case SGEMM_ERR_TIMEOUT: return "a device-side bounded wait ran out";
         case SGEMM_ERR_BAD_ARG: return "invalid argument";
+        case SGEMM_ERR_TOO_LARGE:
+            return "problem needs more than the fixed scratch of sgemm_noalloc "
+                   "(K * round_up(M, 4) floats > 16777216)";
         default: return "unknown status";
     }
 }

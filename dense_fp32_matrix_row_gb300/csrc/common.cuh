@@ -53,6 +53,9 @@ cudaError_t launch_transpose(int64_t M, int64_t K, const float *A, int64_t lda, 
                              int64_t ldt, cudaStream_t stream);
 cudaError_t launch_decode(const GemmArgs &g);
 cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream);
+// Fills g.err, g.wait_ns, g.sm_count and g.encode for the current device
+// (setting the device up on first use); returns an SGEMM_* status.
+int fill_device_args(GemmArgs &g);
 
 
 #ifdef __CUDACC__

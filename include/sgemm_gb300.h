@@ -67,6 +67,7 @@ extern "C" {
 #define SGEMM_ERR_DEVICE     -6   /* the current device is not an sm_103 GPU */
 #define SGEMM_ERR_TIMEOUT    -7   /* a device-side bounded wait ran out (from sgemm_status) */
 #define SGEMM_ERR_BAD_ARG    -8   /* any other invalid argument */
+#define SGEMM_ERR_TOO_LARGE  -9   /* beyond sgemm_noalloc's fixed scratch */
 
 /* Kernel identifiers, for sgemm_select_kernel and sgemm_force_kernel. */
 #define SGEMM_KERNEL_AUTO          0   /* library's choice (sgemm_force_kernel only) */
@@ -167,6 +168,41 @@ int sgemm_selftest_wait(int64_t ns, void *stream);
  * again as needed.  Returns SGEMM_OK or SGEMM_ERR_CUDA.
  */
 int sgemm_release_workspaces(void);
+
+/*
+ * sgemm_noalloc -- sgemm() for callers that must not allocate device memory.
+ *
+ * The reference pages have no counterpart to this entry point; it exists for
+ * users of the library.  sgemm() calls cudaMallocAsync the first time a
+ * stream needs a larger workspace for its transposed copy of A.  Some callers
+ * cannot let any allocation happen: processes whose device memory is all
+ * reserved up front by their own pool or by a host framework that forbids
+ * later allocation, and latency-critical paths that cannot take an
+ * allocation's cost or its possible synchronisation.  sgemm_noalloc computes
+ * the same result with the same kernels, but keeps the transposed copy of A
+ * in a fixed array compiled into the library (a file-scope __device__ array
+ * of 16,777,216 floats, 64 MiB).  It calls no cudaMalloc, cudaMallocAsync,
+ * cudaFree or other allocating routine.
+ *
+ * Limit: shapes sgemm() runs on its FFMA tile kernel (M > 16, B 16-byte
+ * aligned, ldb % 4 == 0) need K * round_up(M, 4) <= 16,777,216 floats
+ * (M = K = 4096 just fits); larger ones return SGEMM_ERR_TOO_LARGE with
+ * nothing enqueued.  All other shapes use no scratch and run as in sgemm().
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current).  Make that first call
+ * before any stream capture.
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents.  Each call overwrites the part it reads before reading it,
+ * so nothing has to be cleared, but calls that overlap on the GPU (on
+ * different streams, or from host threads that do not order their streams)
+ * race on the array: run them on one stream or serialise them.
+ * The array occupies 64 MiB on each GPU where this entry point has been used,
+ * until the process exits.
+ * Arguments, conventions and other errors are those of sgemm().
+ */
+int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
+                  const float *A, int64_t lda, const float *B, int64_t ldb,
+                  float beta, float *C, int64_t ldc, void *stream);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int sgemm_version(void);
