@@ -21,6 +21,8 @@
 //    cluster owns and applies C = alpha*sum + beta*C (C read only if beta != 0).
 #include <cooperative_groups.h>
 
+#include <cmath>
+
 #include "common.cuh"
 
 namespace cg = cooperative_groups;
@@ -54,32 +56,45 @@ __device__ __forceinline__ float4 load_b4(const float *__restrict__ brow, int64_
     return v;
 }
 
+#ifndef DECODE_ORDER
+#define DECODE_ORDER 0
+#endif
+
+// acc[m][c] += A[m][k] * B[k][col + c] for one k row: a is the K-major A row
+// (MT values), b the lane's four columns.  ORDER 0 walks m then c; 1 walks c
+// then m; 2 walks m then c with c reversed on odd m (consecutive FFMAs share
+// an operand across the turn).
 template <int MT>
 __device__ __forceinline__ void fma_row(float (&acc)[MT][4], const float *__restrict__ a,
                                         const float4 &b) {
+    float am[MT];
     if constexpr (MT >= 4) {
 #pragma unroll
         for (int m4 = 0; m4 < MT / 4; ++m4) {
             const float4 av = *reinterpret_cast<const float4 *>(a + 4 * m4);
-            const float am[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float(&r)[4] = acc[4 * m4 + q];
-                r[0] = fmaf(am[q], b.x, r[0]);
-                r[1] = fmaf(am[q], b.y, r[1]);
-                r[2] = fmaf(am[q], b.z, r[2]);
-                r[3] = fmaf(am[q], b.w, r[3]);
-            }
+            am[4 * m4 + 0] = av.x;
+            am[4 * m4 + 1] = av.y;
+            am[4 * m4 + 2] = av.z;
+            am[4 * m4 + 3] = av.w;
         }
     } else {
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            const float am = a[m];
-            acc[m][0] = fmaf(am, b.x, acc[m][0]);
-            acc[m][1] = fmaf(am, b.y, acc[m][1]);
-            acc[m][2] = fmaf(am, b.z, acc[m][2]);
-            acc[m][3] = fmaf(am, b.w, acc[m][3]);
-        }
+        for (int m = 0; m < MT; ++m) am[m] = a[m];
+    }
+    const float bv[4] = {b.x, b.y, b.z, b.w};
+    if (DECODE_ORDER == 1) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[m][c] = fmaf(am[m], bv[c], acc[m][c]);
+    } else {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = (DECODE_ORDER == 2 && (m & 1)) ? 3 - cc : cc;
+                acc[m][c] = fmaf(am[m], bv[c], acc[m][c]);
+            }
     }
 }
 
@@ -198,12 +213,260 @@ cudaError_t launch_mt(const GemmArgs &g) {
                               g.lda, g.B, g.ldb, g.beta, g.C, g.ldc, kslice);
 }
 
+// ---------------------------------------------------------------- TMA-streamed variant
+// B 16-byte aligned with ldb % 4 == 0: B panels of TKB rows x
+// (128*TNV) columns stream through a TSTAGES-deep ring of 2-D TMA copies (one
+// "full" mbarrier per stage), so every block keeps TSTAGES-1 panels in flight
+// independently of its arithmetic.  Each lane owns TNV float4 column groups
+// (columns lane*4 + 128*v), so each broadcast A value it loads from shared
+// memory feeds 4*TNV FFMAs: at M = 16 the shared-memory bytes per byte of B
+// fall from 5 (one float4 per lane) to 3.  Each of the DW warps reads rows
+// warp, warp+DW, ... of a panel; the last warp to release a stage issues the
+// copy that refills it (as in the FFMA kernel).  A's K-slice is staged K-major
+// in shared memory in chunks of KCH rows.  The reduction over warps and over
+// the cluster is the same fixed-order one as above.
+#ifndef DECODE_TKB
+#define DECODE_TKB 32
+#endif
+constexpr int TKB = DECODE_TKB;   // rows of B per stage
+constexpr uint64_t DRAIN_NS = 1000000000ull;
+
+template <int MT, int TNV, int DW, int TSTAGES>
+struct TmaCfg {
+    static constexpr int COLS = 128 * TNV;                                  // columns per cluster
+    static constexpr int THREADS = DW * 32;
+    static constexpr size_t B_STAGE = (size_t)TKB * COLS;                   // floats
+    static constexpr size_t B_RING = TSTAGES * B_STAGE;                     // floats
+    static constexpr size_t RED = (size_t)DW * MT * COLS;                   // floats, aliases the ring
+    static constexpr size_t REGION0 = B_RING > RED ? B_RING : RED;
+    static constexpr size_t AS = (size_t)KCH * MT;                          // floats
+    static constexpr size_t PART = (size_t)MT * COLS;                       // floats
+    static constexpr size_t FLOATS = REGION0 + AS + PART;
+    static constexpr size_t BYTES = 128 + FLOATS * 4 + TSTAGES * 16;
+    static_assert(KCH % TKB == 0 && TKB % DW == 0, "A chunks hold whole B panels");
+    static_assert(COLS <= 256, "TMA box is at most 256 elements wide");
+    static_assert(BYTES <= 227 * 1024, "shared memory per block");
+};
+
+template <class T, int MT, int TNV, int DW, int TSTAGES>
+__global__ void __launch_bounds__(DW * 32, 1)
+decode_tma_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int64_t K,
+                  float alpha, const float *__restrict__ A, int64_t lda, float beta,
+                  float *__restrict__ C, int64_t ldc, int64_t kslice, unsigned *err,
+                  uint64_t wait_ns) {
+    using L = T;
+    constexpr int COLS = L::COLS;
+    extern __shared__ unsigned char smem_raw[];
+    float *smem = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                            ~uintptr_t(127));
+    float *sB = smem;                      // [TSTAGES][TKB][COLS]
+    float *red = smem;                     // [DW][MT][COLS], after the K loop
+    float *As = smem + L::REGION0;         // [KCH][MT]
+    float *part = As + L::AS;              // [MT][COLS]
+    uint64_t *full = reinterpret_cast<uint64_t *>(part + L::PART);
+    unsigned *arrived = reinterpret_cast<unsigned *>(full + TSTAGES);
+    int *issued = reinterpret_cast<int *>(arrived + TSTAGES);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int ks = (int)cluster.num_blocks();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n0 = (int64_t)blockIdx.y * COLS;
+    const int64_t kbeg = (int64_t)rank * kslice;
+    const int64_t kend = (kbeg + kslice < K) ? kbeg + kslice : K;
+    const int nst = kend > kbeg ? (int)((kend - kbeg + TKB - 1) / TKB) : 0;
+
+    auto issue = [&](int st) {
+        const int s = st % TSTAGES;
+        issued[s] = st;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, (uint32_t)(L::B_STAGE * 4));
+        tma_load_2d(smem_u32(sB + s * L::B_STAGE), &tmB, fb, (int32_t)n0,
+                    (int32_t)(kbeg + (int64_t)st * TKB));
+    };
+    auto drain = [&]() {
+        for (int s = 0; s < TSTAGES; ++s) {
+            const int st = *reinterpret_cast<volatile int *>(&issued[s]);
+            if (st >= 0) mbar_wait(smem_u32(&full[s]), (st / TSTAGES) & 1, DRAIN_NS);
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TSTAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            arrived[s] = 0;
+            issued[s] = -1;
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmB);
+        for (int st = 0; st < TSTAGES && st < nst; ++st) issue(st);
+    }
+
+    float acc[TNV][MT][4];
+#pragma unroll
+    for (int v = 0; v < TNV; ++v)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[v][m][0] = acc[v][m][1] = acc[v][m][2] = acc[v][m][3] = 0.0f;
+    bool failed = false;
+
+    for (int st = 0; st < nst; ++st) {
+        const int64_t kc = kbeg + (int64_t)st * TKB;
+        const int64_t chunk0 = kbeg + ((int64_t)st * TKB) / KCH * KCH;
+        if (kc == chunk0) {
+            // Next chunk of A, K-major: As[k - chunk0][m]; rows past kend are zero.
+            __syncthreads();
+            const int64_t clen64 = (kend - chunk0) < KCH ? (kend - chunk0) : KCH;
+            const int clen = (int)clen64;
+            for (int idx = threadIdx.x; idx < KCH * MT; idx += L::THREADS) {
+                const int m = idx / KCH, kl = idx - m * KCH;
+                As[kl * MT + m] = (m < M && kl < clen) ? A[(int64_t)m * lda + chunk0 + kl] : 0.0f;
+            }
+            __syncthreads();
+        }
+        const int s = st % TSTAGES;
+        if (!failed && !mbar_wait(smem_u32(&full[s]), (st / TSTAGES) & 1, wait_ns)) {
+            failed = true;
+            if (lane == 0) {
+                record_error(err, kErrWaitTimeout);
+                drain();
+            }
+        }
+        if (failed) continue;   // keep reaching the block barriers; skip the stage
+        const float *bst = sB + s * L::B_STAGE + lane * 4;
+        const float *ast = As + (kc - chunk0) * MT;
+#pragma unroll
+        for (int j = 0; j < TKB / DW; ++j) {
+            const int r = warp + DW * j;
+#pragma unroll
+            for (int v = 0; v < TNV; ++v) {
+                const float4 b = *reinterpret_cast<const float4 *>(bst + r * COLS + 128 * v);
+                fma_row<MT>(acc[v], ast + r * MT, b);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&arrived[s], 1u) == DW - 1) {
+                arrived[s] = 0;
+                if (st + TSTAGES < nst) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(st + TSTAGES);
+                }
+            }
+        }
+    }
+
+    // Sum over warps in a fixed order; the ring is free once every stage was
+    // read.  (After a time-out, wait for any copy still in flight first.)
+    if (threadIdx.x == 0) drain();
+    const bool any_failed = __syncthreads_or(failed) != 0;
+#pragma unroll
+    for (int v = 0; v < TNV; ++v)
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+            *reinterpret_cast<float4 *>(&red[((size_t)warp * MT + m) * COLS + 128 * v + lane * 4]) =
+                make_float4(acc[v][m][0], acc[v][m][1], acc[v][m][2], acc[v][m][3]);
+    __syncthreads();
+    for (int o = threadIdx.x; o < MT * COLS; o += L::THREADS) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < DW; ++w) sum += red[(size_t)w * MT * COLS + o];
+        part[o] = sum;
+    }
+
+    cluster.sync();
+    const int per = (MT * COLS + ks - 1) / ks;
+    const int obeg = rank * per;
+    const int oend = (obeg + per < MT * COLS) ? obeg + per : MT * COLS;
+    for (int o = obeg + threadIdx.x; o < oend; o += L::THREADS) {
+        float sum = 0.0f;
+        for (int q = 0; q < ks; ++q) sum += cluster.map_shared_rank(part, q)[o];
+        const int m = o / COLS;
+        const int64_t gn = n0 + (o - m * COLS);
+        if (!any_failed && m < M && gn < N) {
+            float *p = C + (int64_t)m * ldc + gn;
+            const float v = alpha * sum;
+            *p = (beta != 0.0f) ? fmaf(beta, *p, v) : v;
+        }
+    }
+    cluster.sync();
+}
+
+// Cluster size: K split over ks blocks (<= 8, a portable cluster), chosen so
+// the grid fills whole waves of resident blocks as nearly as possible.
+inline int choose_ks(int64_t K, int64_t ncb, int slots) {
+    int best = 1;
+    double best_eff = -1.0;
+    for (int ks = 1; ks <= 8; ks *= 2) {
+        if (ks > 1 && K / ks < TKB) break;
+        const double waves = (double)(ncb * ks) / slots;
+        const double eff = waves / std::ceil(waves);
+        // more blocks hide latency better, so prefer larger ks unless clearly worse
+        if (eff > best_eff + 0.02 || (eff > best_eff - 0.02 && ks > best)) {
+            best = ks;
+            best_eff = eff > best_eff ? eff : best_eff;
+        }
+    }
+    return best;
+}
+
+template <int MT, int TNV, int DW, int TSTAGES>
+cudaError_t launch_tma(const GemmArgs &g) {
+    using L = TmaCfg<MT, TNV, DW, TSTAGES>;
+    alignas(64) CUtensorMap tmB;
+    if (!encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, L::COLS, TKB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    auto kern = decode_tma_kernel<L, MT, TNV, DW, TSTAGES>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, L::THREADS, L::BYTES);
+    if (e != cudaSuccess) return e;
+    const int64_t ncb = (g.N + L::COLS - 1) / L::COLS;
+    if (ncb > 65535) return cudaErrorInvalidConfiguration;
+    const int ks = choose_ks(g.K, ncb, (per_sm > 0 ? per_sm : 1) * (g.sm_count > 0 ? g.sm_count : 148));
+    int64_t kslice = (g.K + ks - 1) / ks;
+    kslice = (kslice + TKB - 1) / TKB * TKB;   // whole panels per block
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ks, (unsigned)ncb, 1);
+    cfg.blockDim = dim3(L::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.stream = g.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmB, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha, g.A,
+                              g.lda, g.beta, g.C, g.ldc, kslice, g.err, g.wait_ns);
+}
+
+#ifndef DECODE_TNV
+#define DECODE_TNV 2
+#endif
+#ifndef DECODE_DW
+#define DECODE_DW 8
+#endif
+#ifndef DECODE_STAGES
+#define DECODE_STAGES 3
+#endif
+#ifndef DECODE_TMA_MIN_M
+#define DECODE_TMA_MIN_M 1
+#endif
+
 template <int MT>
 cudaError_t launch_vec(const GemmArgs &g) {
     const bool vec = ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) && (g.ldb % 4 == 0);
+    if (vec && g.M >= DECODE_TMA_MIN_M)
+        return launch_tma<MT, DECODE_TNV, DECODE_DW, DECODE_STAGES>(g);
     return vec ? launch_mt<MT, true>(g) : launch_mt<MT, false>(g);
 }
-
 }  // namespace
 
 cudaError_t launch_decode(const GemmArgs &g) {
