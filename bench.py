@@ -307,13 +307,14 @@ def run_ours(args, world, rank, local):
     dA = torch.from_numpy(A).to(dev)
     dB = torch.from_numpy(B).to(dev)
     dC = torch.from_numpy(C0).to(dev) if C0 is not None else torch.empty((M, N), device=dev)
+    tc = bool(args.tensor_cores)
     kid = sg.select_kernel(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta,
-                           dC.data_ptr(), N, False)
+                           dC.data_ptr(), N, tc)
     # kernels one sgemm() call launches: the FFMA path transposes A first
-    launches_per_call = 2 if kid == sg.KERNEL_FFMA_TMA else 1
+    launches_per_call = {sg.KERNEL_FFMA_TMA: 2, sg.KERNEL_TF32X3: 3}.get(kid, 1)
 
     def step():
-        sg.sgemm(dA, dB, dC, alpha, beta, stream=stream)
+        sg.sgemm(dA, dB, dC, alpha, beta, stream=stream, tensor_cores=tc)
 
     # Parity of this exact launch configuration on sampled rows, before timing.
     with torch.cuda.stream(stream):
@@ -369,7 +370,7 @@ def run_ours(args, world, rank, local):
         dB.copy_(hB, non_blocking=True)
         if beta != 0.0:
             dC.copy_(hC, non_blocking=True)
-        sg.sgemm(dA, dB, dC, alpha, beta, stream=stream)
+        sg.sgemm(dA, dB, dC, alpha, beta, stream=stream, tensor_cores=tc)
         hOut.copy_(dC, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
@@ -455,6 +456,8 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--tensor-cores", action="store_true",
+                    help="time sgemm_3xtf32 instead of sgemm on the main workload")
     ap.add_argument("--print-source-hash", metavar="KERNEL")
     args = ap.parse_args()
     if args.print_source_hash:

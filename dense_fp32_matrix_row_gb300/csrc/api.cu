@@ -162,6 +162,7 @@ bool kernel_can_run(int id, int64_t M, int64_t N, int64_t K, const float *A, int
         case SGEMM_KERNEL_FFMA_TMA: return tma_ok(M, N, K, A, lda, B, ldb);
         case SGEMM_KERNEL_FFMA_GENERIC: return (M + 63) / 64 <= 65535;
         case SGEMM_KERNEL_DECODE: return M <= 16 && (N + 127) / 128 <= 65535;
+        case SGEMM_KERNEL_TF32X3: return tf32x3_can_run(M, N, K);
         default: return false;
     }
 }
@@ -176,7 +177,10 @@ int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t
     const int forced = g_force.load();
     if (forced != SGEMM_KERNEL_AUTO && kernel_can_run(forced, M, N, K, A, lda, B, ldb))
         return forced;
-    (void)tensor;   // the tensor-core kernel is chosen here once it exists
+    // The tensor-core tile is 128 rows tall; skinny products stay on the
+    // (FP32-exact) decode kernel.
+    if (tensor && M > 16 && kernel_can_run(SGEMM_KERNEL_TF32X3, M, N, K, A, lda, B, ldb))
+        return SGEMM_KERNEL_TF32X3;
     if (M <= 16 && kernel_can_run(SGEMM_KERNEL_DECODE, M, N, K, A, lda, B, ldb))
         return SGEMM_KERNEL_DECODE;
     if (tma_ok(M, N, K, A, lda, B, ldb)) return SGEMM_KERNEL_FFMA_TMA;
@@ -215,6 +219,13 @@ int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t ld
                                      g.stream, &ws);
             if (rc != SGEMM_OK) return rc;
             e = launch_ffma_tma(g, ws);
+            break;
+        }
+        case SGEMM_KERNEL_TF32X3: {
+            float *ws = nullptr;
+            const int rc = workspace(tf32x3_workspace_floats(M, N, K) * sizeof(float), g.stream, &ws);
+            if (rc != SGEMM_OK) return rc;
+            e = launch_tf32x3(g, ws);
             break;
         }
         default: return SGEMM_ERR_BAD_ARG;

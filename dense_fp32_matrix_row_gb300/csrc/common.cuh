@@ -53,6 +53,12 @@ cudaError_t launch_transpose(int64_t M, int64_t K, const float *A, int64_t lda, 
                              int64_t ldt, cudaStream_t stream);
 cudaError_t launch_decode(const GemmArgs &g);
 cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream);
+// 3xTF32 tensor-core kernel: splits A and B into TF32 hi/lo parts in
+// `workspace` (tf32x3_workspace_floats(M, N, K) floats), then runs the
+// tcgen05 MMA kernel.
+cudaError_t launch_tf32x3(const GemmArgs &g, float *workspace);
+size_t tf32x3_workspace_floats(int64_t M, int64_t N, int64_t K);
+bool tf32x3_can_run(int64_t M, int64_t N, int64_t K);
 // Fills g.err, g.wait_ns, g.sm_count and g.encode for the current device
 // (setting the device up on first use); returns an SGEMM_* status.
 int fill_device_args(GemmArgs &g);

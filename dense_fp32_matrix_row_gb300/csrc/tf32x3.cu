@@ -1,0 +1,429 @@
+// tf32x3.cu -- FP32-accurate GEMM on the tcgen05 tensor cores (3xTF32).
+//
+// Each operand element x is split into two TF32 numbers,
+//     hi = tf32(x)   and   lo = tf32(x - hi)   (round to nearest),
+// so x = hi + lo up to the 2^-22 relative error of lo; the product is
+// accumulated as  hi*hi + hi*lo + lo*hi  in FP32 (the lo*lo term, below
+// FP32 precision, is dropped) -- the error-compensated "3xTF32" split of
+// Ootomo and Yokota (2022).  The pages only name tensor cores and TF32
+// ("CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", results-table note;
+// "GPU GEMM 优化完全拆解（一）", series outline); this kernel is the FP32-accuracy
+// tensor path the benchmark asks for.
+//
+// Two passes:
+//  1. split kernels (memory-bound) write A_hi, A_lo as [M][K] and B_hi, B_lo
+//     transposed as [N][K] into the workspace, so both MMA operands are
+//     K-major -- the canonical UMMA layout;
+//  2. the MMA kernel: one CTA per 128 x 256 tile of C.  Warp 8 streams 16-wide
+//     K slices of the four operand tiles into a 4-stage shared-memory ring
+//     with TMA (64-byte swizzle); one thread of warp 9 issues, per 8-wide k
+//     step, three tcgen05.mma kind::tf32 (hi*lo, lo*hi, hi*hi) into one FP32
+//     accumulator of 128 lanes x 256 columns in tensor memory and releases
+//     each stage with tcgen05.commit; warps 0-7 read the accumulator back with
+//     tcgen05.ld (each warp 32 lanes = rows, half the columns), add it into
+//     FP32 registers chunk by chunk (see tf32x3_kernel) and finally apply
+//     C = alpha*acc + beta*C, reading C only when beta != 0.
+//
+// Every wait is bounded.  On a time-out the kernel records the error, waits
+// (bounded) for its own TMA copies and MMAs in flight, frees its tensor
+// memory and exits without storing.
+#include "common.cuh"
+
+namespace sgemm_gb300 {
+namespace {
+
+constexpr int TBM = 128, TBN = 256, TBK = 16, TSTG = 4;
+constexpr int KC_TILES = 4;                     // k-tiles per accumulation chunk (64 k)
+constexpr int EPI_WARPS = 8;                    // two warpgroups: 32 rows x 128 columns each
+constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
+constexpr int THREADS = (EPI_WARPS + 2) * 32;
+constexpr int EPI_COLS = TBN / (EPI_WARPS / 4); // columns per epilogue thread
+constexpr int RASTER_GROUP = 16;                // M tiles walked together (L2 reuse)
+constexpr uint32_t A_TILE = TBM * TBK * 4;                 // 8 KB
+constexpr uint32_t B_TILE = TBN * TBK * 4;                 // 16 KB
+constexpr uint32_t STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;  // 48 KB
+constexpr uint32_t TMEM_COLS = 2 * TBN;                    // two 128 x 256 FP32 accumulators
+constexpr size_t SMEM = 1024 + (size_t)TSTG * STAGE_BYTES + 256;
+constexpr uint64_t DRAIN_NS = 1000000000ull;
+static_assert(TBK * 4 == 64, "rows of a K slice fill exactly one 64-byte swizzle span");
+static_assert(A_TILE % 1024 == 0 && B_TILE % 1024 == 0, "tiles keep 1024-byte alignment");
+static_assert(EPI_WARPS % 4 == 0 && EPI_COLS % 16 == 0, "epilogue covers all lanes and columns");
+
+// Instruction descriptor of tcgen05.mma kind::tf32: D format F32 (bits 4-5 = 1),
+// A and B format TF32 (bits 7-9 and 10-12 = 2), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(TBN >> 3) << 17) |
+                           ((uint32_t)(TBM >> 4) << 24);
+
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA
+// with the 64-byte swizzle: rows of 64 bytes, 8-row core groups 512 bytes
+// apart (stride byte offset), descriptor version 1, layout SWIZZLE_64B (4).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);           // start address
+    d |= (uint64_t)1 << 16;                            // leading byte offset (unused here)
+    d |= (uint64_t)((512u >> 4) & 0x3FFFu) << 32;      // stride byte offset
+    d |= (uint64_t)1 << 46;                            // version
+    d |= (uint64_t)4 << 61;                            // SWIZZLE_64B
+    return d;
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+// The mbarrier completes once every tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Chunked accumulation.  A tensor-core MMA adds its products into the FP32
+// accumulator with an error of a fraction of an ulp of the accumulator, so a
+// single accumulator over all of K loses accuracy linearly in K (measured:
+// relative error 1.8e-6 at K = 256 growing to 5.7e-5 at K = 8192).  The MMA
+// thread therefore restarts the accumulator every KC_TILES k-tiles, in two
+// alternating tensor-memory buffers, and the epilogue warps add each chunk
+// into FP32 registers (round to nearest) while the next chunk is computed.
+__global__ void __launch_bounds__(THREADS, 1)
+tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
+              const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
+              int M, int N, int K, float alpha, float beta, float *__restrict__ C, int64_t ldc,
+              int c_vec4, unsigned *err, uint64_t wait_ns) {
+    extern __shared__ unsigned char smem_raw[];
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+    unsigned char *ring = reinterpret_cast<unsigned char *>(base);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)TSTG * STAGE_BYTES);
+    uint64_t *empty = full + TSTG;
+    uint64_t *cfull = empty + TSTG;     // [2] chunk in tensor memory buffer b is complete
+    uint64_t *cempty = cfull + 2;       // [2] epilogue has read buffer b
+    uint64_t *drainbar = cempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drainbar + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Grouped rasterisation: RASTER_GROUP M-tiles x all N-tiles per group, so
+    // the blocks resident at one time share a few A and B panels through L2.
+    const int num_m = (M + TBM - 1) / TBM, num_n = (N + TBN - 1) / TBN;
+    const int pid = blockIdx.x;
+    const int per_group = RASTER_GROUP * num_n;
+    const int first_m = (pid / per_group) * RASTER_GROUP;
+    const int gsz = (num_m - first_m) < RASTER_GROUP ? (num_m - first_m) : RASTER_GROUP;
+    const int tile_m = first_m + (pid % per_group) % gsz;
+    const int tile_n = (pid % per_group) / gsz;
+    const int m0 = tile_m * TBM, n0 = tile_n * TBN;
+    const int ktiles = (K + TBK - 1) / TBK;
+    const int nchunks = (ktiles + KC_TILES - 1) / KC_TILES;
+    auto stage_ptr = [&](int s, int which) -> uint32_t {   // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
+        const uint32_t off = which < 2 ? which * A_TILE : 2 * A_TILE + (which - 2) * B_TILE;
+        return smem_u32(ring + (size_t)s * STAGE_BYTES + off);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TSTG; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&cfull[b]), 1);
+            mbar_init(smem_u32(&cempty[b]), EPI_WARPS);
+        }
+        mbar_init(smem_u32(drainbar), 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) {   // one full warp allocates the accumulator columns
+        __syncwarp();
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    if (warp == PRODUCER_WARP) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmAhi);
+            tma_prefetch_desc(&tmAlo);
+            tma_prefetch_desc(&tmBhi);
+            tma_prefetch_desc(&tmBlo);
+            int kt = 0;
+            for (; kt < ktiles; ++kt) {
+                const int s = kt % TSTG;
+                const uint32_t use = kt / TSTG;
+                if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, wait_ns)) break;
+                const uint32_t fb = smem_u32(&full[s]);
+                mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                tma_load_2d(stage_ptr(s, 0), &tmAhi, fb, kt * TBK, m0);
+                tma_load_2d(stage_ptr(s, 1), &tmAlo, fb, kt * TBK, m0);
+                tma_load_2d(stage_ptr(s, 2), &tmBhi, fb, kt * TBK, n0);
+                tma_load_2d(stage_ptr(s, 3), &tmBlo, fb, kt * TBK, n0);
+            }
+            if (kt < ktiles) {
+                record_error(err, kErrWaitTimeout);
+                for (int q = (kt > TSTG ? kt - TSTG : 0); q < kt; ++q)
+                    mbar_wait(smem_u32(&full[q % TSTG]), (q / TSTG) & 1, DRAIN_NS);
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            bool ok = true;
+            bool issued_any = false;
+            for (int c = 0; c < nchunks && ok; ++c) {
+                const int b = c & 1;
+                if (c >= 2) {   // the epilogue must have read this buffer's previous chunk
+                    if (!mbar_wait(smem_u32(&cempty[b]), ((c >> 1) - 1) & 1, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                const uint32_t d = tmem + (uint32_t)(b * TBN);
+                const int kt_end = (c + 1) * KC_TILES < ktiles ? (c + 1) * KC_TILES : ktiles;
+                for (int kt = c * KC_TILES; kt < kt_end; ++kt) {
+                    const int s = kt % TSTG;
+                    if (!mbar_wait(smem_u32(&full[s]), (kt / TSTG) & 1, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < TBK / 8; ++kk) {
+                        const uint32_t koff = kk * 32;   // 8 TF32 = 32 bytes along K
+                        const uint64_t ahi = smem_desc_sw64(stage_ptr(s, 0) + koff);
+                        const uint64_t alo = smem_desc_sw64(stage_ptr(s, 1) + koff);
+                        const uint64_t bhi = smem_desc_sw64(stage_ptr(s, 2) + koff);
+                        const uint64_t blo = smem_desc_sw64(stage_ptr(s, 3) + koff);
+                        const uint32_t acc_in = (kt != c * KC_TILES || kk != 0) ? 1u : 0u;
+                        tc_mma_tf32(d, ahi, blo, acc_in);
+                        tc_mma_tf32(d, alo, bhi, 1u);
+                        tc_mma_tf32(d, ahi, bhi, 1u);
+                    }
+                    issued_any = true;
+                    tc_commit(smem_u32(&empty[s]));   // the stage is free once these MMAs are done
+                }
+                if (ok) tc_commit(smem_u32(&cfull[b]));
+            }
+            if (!ok) {
+                record_error(err, kErrWaitTimeout);
+                if (issued_any) {   // wait for the MMAs already issued
+                    tc_commit(smem_u32(drainbar));
+                    mbar_wait(smem_u32(drainbar), 0, DRAIN_NS);
+                }
+            }
+        }
+    } else {
+        // Epilogue warp w: tensor-memory lanes (rows) 32*(w%4) .. +31,
+        // columns (w/4)*EPI_COLS .. +EPI_COLS.
+        const int lane_base = (warp & 3) * 32;
+        const int col_base = (warp >> 2) * EPI_COLS;
+        float acc[EPI_COLS];
+#pragma unroll
+        for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+        bool ok = true;
+        for (int c = 0; c < nchunks; ++c) {
+            const int b = c & 1;
+            // tcgen05.ld is warp-collective: lane 0 decides for the warp whether
+            // the chunk is ready; the others then see the completed phase at once.
+            bool ready = lane == 0 ? mbar_wait(smem_u32(&cfull[b]), (c >> 1) & 1, wait_ns) : false;
+            ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+            if (!ready) {
+                ok = false;
+                break;
+            }
+            mbar_wait(smem_u32(&cfull[b]), (c >> 1) & 1, DRAIN_NS);
+            tc_fence_after();
+            const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + (uint32_t)(b * TBN + col_base);
+#pragma unroll
+            for (int piece = 0; piece < EPI_COLS / 16; ++piece) {
+                float v[16];
+                __syncwarp();
+                tc_ld16(taddr + (uint32_t)(piece * 16), v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[piece * 16 + i] += v[i];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&cempty[b]));
+        }
+        if (!ok) {
+            if (lane == 0) record_error(err, kErrWaitTimeout);
+        } else {
+            const int gm = m0 + lane_base + lane;
+            if (gm < M) {
+                float *crow = C + (int64_t)gm * ldc;
+#pragma unroll
+                for (int q = 0; q < EPI_COLS / 4; ++q) {
+                    const int gn = n0 + col_base + 4 * q;
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = alpha * acc[4 * q + e];
+                    if (c_vec4 && gn + 3 < N) {
+                        float4 *p = reinterpret_cast<float4 *>(crow + gn);
+                        if (beta != 0.0f) {
+                            const float4 cv = *p;
+                            o[0] = fmaf(beta, cv.x, o[0]);
+                            o[1] = fmaf(beta, cv.y, o[1]);
+                            o[2] = fmaf(beta, cv.z, o[2]);
+                            o[3] = fmaf(beta, cv.w, o[3]);
+                        }
+                        *p = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (gn + e < N) {
+                                float *p = crow + gn + e;
+                                *p = (beta != 0.0f) ? fmaf(beta, *p, o[e]) : o[e];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- split passes
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// hi/lo split of an R x Cc row-major matrix into two [R][ldo] arrays.
+__global__ void __launch_bounds__(256)
+split_rows_kernel(int64_t R, int64_t Cc, const float *__restrict__ X, int64_t ldx,
+                  float *__restrict__ hi, float *__restrict__ lo, int64_t ldo) {
+    for (int64_t r = blockIdx.y; r < R; r += gridDim.y) {
+        for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < Cc;
+             c += (int64_t)gridDim.x * blockDim.x) {
+            const float x = X[r * ldx + c];
+            const float h = tf32_rna(x);
+            hi[r * ldo + c] = h;
+            lo[r * ldo + c] = tf32_rna(x - h);
+        }
+    }
+}
+
+// hi/lo split of B (K x N, row-major) written transposed: hi[n][k], lo[n][k].
+constexpr int TT = 32, TROWS = 8;
+__global__ void __launch_bounds__(TT *TROWS)
+split_transpose_kernel(int64_t K, int64_t N, const float *__restrict__ B, int64_t ldb,
+                       float *__restrict__ hi, float *__restrict__ lo, int64_t ldo) {
+    __shared__ float tile[TT][TT + 1];
+    const int64_t n0 = (int64_t)blockIdx.x * TT, k0 = (int64_t)blockIdx.y * TT;
+    const int tx = threadIdx.x, ty = threadIdx.y;
+#pragma unroll
+    for (int r = ty; r < TT; r += TROWS) {
+        const int64_t k = k0 + r, n = n0 + tx;
+        if (k < K && n < N) tile[r][tx] = B[k * ldb + n];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = ty; r < TT; r += TROWS) {
+        const int64_t n = n0 + r, k = k0 + tx;
+        if (n < N && k < K) {
+            const float x = tile[tx][r];
+            const float h = tf32_rna(x);
+            hi[n * ldo + k] = h;
+            lo[n * ldo + k] = tf32_rna(x - h);
+        }
+    }
+}
+
+}  // namespace
+
+int64_t tf32x3_ld(int64_t K) { return (K + 3) / 4 * 4; }
+
+size_t tf32x3_workspace_floats(int64_t M, int64_t N, int64_t K) {
+    const int64_t ldk = tf32x3_ld(K);
+    const int64_t a = (M * ldk + 63) / 64 * 64, b = (N * ldk + 63) / 64 * 64;
+    return (size_t)(2 * a + 2 * b);
+}
+
+bool tf32x3_can_run(int64_t M, int64_t N, int64_t K) {
+    const int64_t lim = int64_t(1) << 31;
+    return M < lim && N < lim && K < lim && ((M + TBM - 1) / TBM) * ((N + TBN - 1) / TBN) <= 0x7fffffff &&
+           (K + 31) / 32 <= 65535;
+}
+
+cudaError_t launch_tf32x3(const GemmArgs &g, float *ws) {
+    const int64_t ldk = tf32x3_ld(g.K);
+    const int64_t asz = (g.M * ldk + 63) / 64 * 64, bsz = (g.N * ldk + 63) / 64 * 64;
+    float *ahi = ws, *alo = ws + asz, *bhi = ws + 2 * asz, *blo = ws + 2 * asz + bsz;
+
+    {   // split A (rows stay rows), split + transpose B
+        const int64_t gx = (g.K + 255) / 256;
+        const dim3 grid((unsigned)(gx < 64 ? gx : 64), (unsigned)(g.M < 65535 ? g.M : 65535));
+        split_rows_kernel<<<grid, 256, 0, g.stream>>>(g.M, g.K, g.A, g.lda, ahi, alo, ldk);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const int64_t tx = (g.N + TT - 1) / TT, ty = (g.K + TT - 1) / TT;
+        if (ty > 65535 || tx > 0x7fffffff) return cudaErrorInvalidConfiguration;
+        split_transpose_kernel<<<dim3((unsigned)tx, (unsigned)ty), dim3(TT, TROWS), 0, g.stream>>>(
+            g.K, g.N, g.B, g.ldb, bhi, blo, ldk);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+
+    alignas(64) CUtensorMap tAhi, tAlo, tBhi, tBlo;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_tma_2d(g.encode, &tAhi, ahi, g.K, g.M, ldk, TBK, TBM, sw) ||
+        !encode_tma_2d(g.encode, &tAlo, alo, g.K, g.M, ldk, TBK, TBM, sw) ||
+        !encode_tma_2d(g.encode, &tBhi, bhi, g.K, g.N, ldk, TBK, TBN, sw) ||
+        !encode_tma_2d(g.encode, &tBlo, blo, g.K, g.N, ldk, TBK, TBN, sw))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SMEM);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = ((g.N + TBN - 1) / TBN) * ((g.M + TBM - 1) / TBM);
+    if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)tiles);
+    const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
+    tf32x3_kernel<<<grid, THREADS, SMEM, g.stream>>>(tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N,
+                                                     (int)g.K, g.alpha, g.beta, g.C, g.ldc, c_vec4,
+                                                     g.err, g.wait_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace sgemm_gb300

@@ -107,8 +107,11 @@ int sgemm(int64_t M, int64_t N, int64_t K, float alpha,
  * kernel accumulates hi*hi + hi*lo + lo*hi in FP32 tensor memory, which keeps
  * single-precision accuracy (the 3xTF32 error-compensated split of Ootomo and
  * Yokota, 2022).  Arguments, conventions and errors are those of sgemm().
- * Shapes the tensor-core kernel does not take (misaligned pointers or ld,
- * M <= 16) run sgemm()'s FFMA kernels instead.
+ * The operands are split into a workspace first (A as [M][K] hi/lo
+ * arrays, B transposed to [N][K] hi/lo arrays: 2*(M+N)*round_up(K,4)
+ * floats, grown like sgemm()'s workspace), so any alignment and ld are
+ * accepted.  Skinny products (M <= 16) run sgemm()'s decode kernel.
+ * Infinite inputs give NaN on this path (hi - inf is not finite).
  */
 int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha,
                  const float *A, int64_t lda, const float *B, int64_t ldb,

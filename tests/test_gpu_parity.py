@@ -258,3 +258,74 @@ def test_workload_large_sampled_rows(name):
     A, B, C0, w = synth.workload_inputs(name)
     C0 = np.full((w["M"], w["N"]), np.nan, np.float32) if C0 is None else C0
     run_checked(sg, A, B, C0, w["alpha"], w["beta"], rows=_sample_rows(w["M"]))
+
+
+# ---------------------------------------------------------------- 3xTF32 tensor-core path
+TF = sg.KERNEL_TF32X3
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 5, 3), (128, 256, 16), (129, 257, 33), (300, 260, 100),
+                                   (255, 513, 1000), (1000, 300, 4097), (17, 1, 1)])
+def test_tf32x3_shapes(M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "uniform", seed=M * 7 + N + K, beta=0.5)
+    _, chosen = run_checked(sg, A, B, C0, 1.25, 0.5, tensor_cores=True)
+    assert chosen == TF
+
+
+def test_tf32x3_small_integers_exact():
+    # integers in [-4, 4] are exact TF32 numbers (lo = 0) and every partial sum
+    # stays below 2^24, so the tensor-core result is exact
+    A, B, C0 = make_inputs(300, 200, 1000, "int", seed=5, beta=-2.0)
+    run_checked(sg, A, B, C0, 3.0, -2.0, tensor_cores=True, exact=True)
+
+
+def test_tf32x3_alpha_beta_and_layouts():
+    M, N, K = 70, 45, 33
+    A, B, C0 = make_inputs(M, N, K, "int", seed=12, beta=1.0)
+    for alpha, beta in [(1.0, 0.0), (1.0, 1.0), (-1.0, 0.5), (0.0, 3.0), (2.0, -1.0)]:
+        c = C0 if beta != 0.0 else np.full((M, N), np.nan, np.float32)
+        run_checked(sg, A, B, c, alpha, beta, tensor_cores=True, exact=True)
+    for lds, offsets in [((37, 47, 46), (1, 3, 1)), ((40, 48, 48), (0, 0, 0))]:
+        run_checked(sg, A, B, C0, 1.0, 1.0, lds=lds, offsets=offsets, tensor_cores=True,
+                    exact=True)
+
+
+def test_tf32x3_is_three_term():
+    """Inputs with 24 significant bits: one TF32 product keeps 11, so a 1xTF32
+    result misses the 1e-6 gate here by an order of magnitude; the 3xTF32
+    result must stay within a few times the FP32 FFMA error."""
+    from gpu_util import normwise_err
+    import oracle
+    M, N, K = 256, 256, 2048
+    A, B, _ = make_inputs(M, N, K, "uniform", seed=77)
+    ref = oracle.sgemm(A, B)
+    errs = {}
+    for tc in (False, True):
+        dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        dC = torch.empty((M, N), device="cuda")
+        sg.sgemm(dA, dB, dC, 1.0, 0.0, tensor_cores=tc)
+        assert sg.status() == sg.OK
+        errs[tc] = normwise_err(dC.cpu().numpy(), ref, A, B, K)
+    # one-term TF32 would be ~2^-11 / sqrt(K) relative, about 1e-5 on this gate
+    assert errs[True] <= 4 * errs[False] + 1e-9, errs
+    assert errs[True] < 1e-7, errs
+
+
+def test_tf32x3_nan_propagates():
+    M, N, K = 140, 64, 64
+    A, B, _ = make_inputs(M, N, K, "uniform", seed=3)
+    A[7, 9] = np.nan
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.zeros((M, N), device="cuda")
+    sg.sgemm(dA, dB, dC, 1.0, 0.0, tensor_cores=True)
+    assert sg.status() == sg.OK
+    C = dC.cpu().numpy()
+    assert np.isnan(C[7]).all() and np.isfinite(np.delete(C, 7, axis=0)).all()
+
+
+def test_workload_8192_3xtf32_sampled_rows():
+    A, B, C0, w = synth.workload_inputs("sgemm_8192")
+    C0 = np.full((w["M"], w["N"]), np.nan, np.float32)
+    _, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"], tensor_cores=True,
+                            rows=_sample_rows(w["M"]))
+    assert chosen == TF
