@@ -150,13 +150,22 @@ def dist_setup():
 
 
 def barrier_max(value: float, world: int, device=None) -> float:
+    """Max of `value` over all ranks (a timing scalar, not data).  Works on the
+    NCCL group the bench uses on GPUs and on a gloo group (CPU tensors)."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
+    if dist.get_backend() != "nccl":
+        device = "cpu"
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: the work of every rank over the slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms * 1e-3) / 1e12
 
 
 def time_oracle(M, N, K, alpha, beta, A, B, C0, budget_s: float, threads: int = 0):
@@ -362,7 +371,7 @@ def run_ours(args, world, rank, local):
         raise SystemExit(f"kernel status {sg.status_string(st)}")
     total_ms = barrier_max(total_ms, world, dev)
     flops = acc.gemm_flops(M, N, K)
-    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = aggregate_tflops(flops, args.steps, world, total_ms)
 
     # End to end: pinned host buffers, H2D of A, B, C and D2H of C each step.
     hA = torch.from_numpy(A).pin_memory()
@@ -385,7 +394,7 @@ def run_ours(args, world, rank, local):
         torch.cuda.synchronize()
         e2e_ms, _ = timed_steps(e2e_step, e2e_steps, stream)
     e2e_ms = barrier_max(e2e_ms, world, dev)
-    e2e_value = flops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+    e2e_value = aggregate_tflops(flops, e2e_steps, world, e2e_ms)
     h2d = 4 * (M * K + K * N + (M * N if beta != 0.0 else 0))
     d2h = 4 * M * N
 
