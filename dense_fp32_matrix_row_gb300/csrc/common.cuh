@@ -48,9 +48,15 @@ cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace);
 int64_t ffma_tma_at_ld(int64_t M);
 // Largest M the TMA FFMA kernel's grid can cover.
 int64_t ffma_tma_max_m();
-// At[k*ldt + m] = A[m*lda + k] for m < M, k < K.
+// At[k*ldt + m] = A[m*lda + k] for m < M, k < K (ldt % 4 == 0, At 16-byte aligned).
 cudaError_t launch_transpose(int64_t M, int64_t K, const float *A, int64_t lda, float *At,
                              int64_t ldt, cudaStream_t stream);
+// TF32 hi/lo split of B (K x N) written transposed: hi[n*ldo + k], lo[n*ldo + k].
+cudaError_t launch_transpose_split(int64_t K, int64_t N, const float *B, int64_t ldb, float *hi,
+                                   float *lo, int64_t ldo, cudaStream_t stream);
+// TF32 hi/lo split of X (R x Cc) in place of layout: hi[r*ldo + c], lo[r*ldo + c].
+cudaError_t launch_split_rows(int64_t R, int64_t Cc, const float *X, int64_t ldx, float *hi,
+                              float *lo, int64_t ldo, cudaStream_t stream);
 cudaError_t launch_decode(const GemmArgs &g);
 cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream);
 // 3xTF32 tensor-core kernel: splits A and B into TF32 hi/lo parts in

@@ -56,14 +56,8 @@ __device__ __forceinline__ float4 load_b4(const float *__restrict__ brow, int64_
     return v;
 }
 
-#ifndef DECODE_ORDER
-#define DECODE_ORDER 0
-#endif
-
 // acc[m][c] += A[m][k] * B[k][col + c] for one k row: a is the K-major A row
-// (MT values), b the lane's four columns.  ORDER 0 walks m then c; 1 walks c
-// then m; 2 walks m then c with c reversed on odd m (consecutive FFMAs share
-// an operand across the turn).
+// (MT values), b the lane's four columns.
 template <int MT>
 __device__ __forceinline__ void fma_row(float (&acc)[MT][4], const float *__restrict__ a,
                                         const float4 &b) {
@@ -82,20 +76,10 @@ __device__ __forceinline__ void fma_row(float (&acc)[MT][4], const float *__rest
         for (int m = 0; m < MT; ++m) am[m] = a[m];
     }
     const float bv[4] = {b.x, b.y, b.z, b.w};
-    if (DECODE_ORDER == 1) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+    for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int m = 0; m < MT; ++m) acc[m][c] = fmaf(am[m], bv[c], acc[m][c]);
-    } else {
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c = (DECODE_ORDER == 2 && (m & 1)) ? 3 - cc : cc;
-                acc[m][c] = fmaf(am[m], bv[c], acc[m][c]);
-            }
-    }
+        for (int c = 0; c < 4; ++c) acc[m][c] = fmaf(am[m], bv[c], acc[m][c]);
 }
 
 template <int MT, bool VEC>
@@ -228,6 +212,9 @@ cudaError_t launch_mt(const GemmArgs &g) {
 #ifndef DECODE_TKB
 #define DECODE_TKB 32
 #endif
+#ifndef DECODE_MINB
+#define DECODE_MINB 1
+#endif
 constexpr int TKB = DECODE_TKB;   // rows of B per stage
 constexpr uint64_t DRAIN_NS = 1000000000ull;
 
@@ -249,7 +236,7 @@ struct TmaCfg {
 };
 
 template <class T, int MT, int TNV, int DW, int TSTAGES>
-__global__ void __launch_bounds__(DW * 32, 1)
+__global__ void __launch_bounds__(DW * 32, DECODE_MINB)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int64_t K,
                   float alpha, const float *__restrict__ A, int64_t lda, float beta,
                   float *__restrict__ C, int64_t ldc, int64_t kslice, unsigned *err,
@@ -382,8 +369,14 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int
     const int obeg = rank * per;
     const int oend = (obeg + per < MT * COLS) ? obeg + per : MT * COLS;
     for (int o = obeg + threadIdx.x; o < oend; o += L::THREADS) {
+        // the (up to 8) remote loads are independent: issue them together,
+        // then add in rank order
+        float pv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pv[q] = q < ks ? cluster.map_shared_rank(part, q)[o] : 0.0f;
         float sum = 0.0f;
-        for (int q = 0; q < ks; ++q) sum += cluster.map_shared_rank(part, q)[o];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum += pv[q];
         const int m = o / COLS;
         const int64_t gn = n0 + (o - m * COLS);
         if (!any_failed && m < M && gn < N) {

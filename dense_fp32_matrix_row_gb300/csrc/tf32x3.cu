@@ -323,54 +323,6 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__
     }
 }
 
-// ---------------------------------------------------------------- split passes
-__device__ __forceinline__ float tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
-// hi/lo split of an R x Cc row-major matrix into two [R][ldo] arrays.
-__global__ void __launch_bounds__(256)
-split_rows_kernel(int64_t R, int64_t Cc, const float *__restrict__ X, int64_t ldx,
-                  float *__restrict__ hi, float *__restrict__ lo, int64_t ldo) {
-    for (int64_t r = blockIdx.y; r < R; r += gridDim.y) {
-        for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < Cc;
-             c += (int64_t)gridDim.x * blockDim.x) {
-            const float x = X[r * ldx + c];
-            const float h = tf32_rna(x);
-            hi[r * ldo + c] = h;
-            lo[r * ldo + c] = tf32_rna(x - h);
-        }
-    }
-}
-
-// hi/lo split of B (K x N, row-major) written transposed: hi[n][k], lo[n][k].
-constexpr int TT = 32, TROWS = 8;
-__global__ void __launch_bounds__(TT *TROWS)
-split_transpose_kernel(int64_t K, int64_t N, const float *__restrict__ B, int64_t ldb,
-                       float *__restrict__ hi, float *__restrict__ lo, int64_t ldo) {
-    __shared__ float tile[TT][TT + 1];
-    const int64_t n0 = (int64_t)blockIdx.x * TT, k0 = (int64_t)blockIdx.y * TT;
-    const int tx = threadIdx.x, ty = threadIdx.y;
-#pragma unroll
-    for (int r = ty; r < TT; r += TROWS) {
-        const int64_t k = k0 + r, n = n0 + tx;
-        if (k < K && n < N) tile[r][tx] = B[k * ldb + n];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = ty; r < TT; r += TROWS) {
-        const int64_t n = n0 + r, k = k0 + tx;
-        if (n < N && k < K) {
-            const float x = tile[tx][r];
-            const float h = tf32_rna(x);
-            hi[n * ldo + k] = h;
-            lo[n * ldo + k] = tf32_rna(x - h);
-        }
-    }
-}
-
 }  // namespace
 
 int64_t tf32x3_ld(int64_t K) { return (K + 3) / 4 * 4; }
@@ -392,19 +344,11 @@ cudaError_t launch_tf32x3(const GemmArgs &g, float *ws) {
     const int64_t asz = (g.M * ldk + 63) / 64 * 64, bsz = (g.N * ldk + 63) / 64 * 64;
     float *ahi = ws, *alo = ws + asz, *bhi = ws + 2 * asz, *blo = ws + 2 * asz + bsz;
 
-    {   // split A (rows stay rows), split + transpose B
-        const int64_t gx = (g.K + 255) / 256;
-        const dim3 grid((unsigned)(gx < 64 ? gx : 64), (unsigned)(g.M < 65535 ? g.M : 65535));
-        split_rows_kernel<<<grid, 256, 0, g.stream>>>(g.M, g.K, g.A, g.lda, ahi, alo, ldk);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        const int64_t tx = (g.N + TT - 1) / TT, ty = (g.K + TT - 1) / TT;
-        if (ty > 65535 || tx > 0x7fffffff) return cudaErrorInvalidConfiguration;
-        split_transpose_kernel<<<dim3((unsigned)tx, (unsigned)ty), dim3(TT, TROWS), 0, g.stream>>>(
-            g.K, g.N, g.B, g.ldb, bhi, blo, ldk);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
+    // split A (rows stay rows), split + transpose B
+    cudaError_t e = launch_split_rows(g.M, g.K, g.A, g.lda, ahi, alo, ldk, g.stream);
+    if (e != cudaSuccess) return e;
+    e = launch_transpose_split(g.K, g.N, g.B, g.ldb, bhi, blo, ldk, g.stream);
+    if (e != cudaSuccess) return e;
 
     alignas(64) CUtensorMap tAhi, tAlo, tBhi, tBlo;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
@@ -413,8 +357,7 @@ cudaError_t launch_tf32x3(const GemmArgs &g, float *ws) {
         !encode_tma_2d(g.encode, &tBhi, bhi, g.K, g.N, ldk, TBK, TBN, sw) ||
         !encode_tma_2d(g.encode, &tBlo, blo, g.K, g.N, ldk, TBK, TBN, sw))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM);
+    e = cudaFuncSetAttribute(tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
     if (e != cudaSuccess) return e;
     const int64_t tiles = ((g.N + TBN - 1) / TBN) * ((g.M + TBM - 1) / TBM);
     if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;

@@ -1,50 +1,178 @@
-// transpose.cu -- At[k][m] = A[m][k] for the FFMA kernel's A operand.
+// transpose.cu -- memory-bound operand preparation passes.
 //
-// The FFMA kernel reads A as K-major tiles ([k][m]: four consecutive rows in
-// one 128-bit shared load), the layout the pages reach by transposing A on its
-// way into shared memory ("CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS",
-// section "7. Kernel 6"; "GPU 基础原理", section 4.3, load-and-transpose).  TMA
-// cannot transpose 4-byte elements, so this memory-bound pass writes A^T once
-// into a workspace, and every CTA then stages K-major A tiles with TMA.
+//  * launch_transpose:       At[k][m] = A[m][k] (the FFMA kernel's K-major A);
+//  * launch_transpose_split: hi[n][k] = tf32(B[k][n]), lo[n][k] = tf32(B[k][n] - hi)
+//                            (the 3xTF32 kernel's K-major B halves);
+//  * launch_split_rows:      hi[r][c] = tf32(X[r][c]), lo[r][c] = tf32(X[r][c] - hi)
+//                            (the 3xTF32 kernel's A halves).
 //
-// 32x32 tiles through padded shared memory: reads are coalesced along k, writes
-// along m.  Any A alignment and any lda are accepted (plain 4-byte loads);
-// the output row stride ldt is a multiple of 4 floats so TMA can read it.
+// The FFMA kernel reads A as K-major tiles (four consecutive rows in one
+// 128-bit shared load), the layout the pages reach by transposing A on its way
+// into shared memory ("CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section
+// "7. Kernel 6"; "GPU 基础原理", section 4.3, load-and-transpose).  TMA cannot
+// transpose 4-byte elements, so these passes write the transposed operand once
+// and every CTA then stages K-major tiles with TMA.
+//
+// Transposes go through 64 x 64 shared-memory tiles: 128-bit loads along the
+// source rows, 128-bit stores along the destination rows, scalar accesses
+// only where a source row is unaligned or a tile is cut by the matrix edge.
+// Destination row strides are multiples of 4 floats.
 #include "common.cuh"
 
 namespace sgemm_gb300 {
 namespace {
 
-constexpr int TT = 32;       // tile edge
-constexpr int TROWS = 8;     // block is TT x TROWS threads
+constexpr int TD = 64;            // tile edge
+constexpr int TTHREADS = 256;     // 16 float4 columns x 16 rows per pass
 
-__global__ void __launch_bounds__(TT *TROWS)
-transpose_kernel(int64_t M, int64_t K, const float *__restrict__ A, int64_t lda,
-                 float *__restrict__ At, int64_t ldt) {
-    __shared__ float tile[TT][TT + 1];
-    const int64_t k0 = (int64_t)blockIdx.x * TT, m0 = (int64_t)blockIdx.y * TT;
-    const int tx = threadIdx.x, ty = threadIdx.y;
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// dst[c][r] (= dst_hi / dst_lo split when SPLIT) from src[r][c], R x Cc source.
+template <bool SPLIT>
+__global__ void __launch_bounds__(TTHREADS)
+transpose_tile_kernel(int64_t R, int64_t Cc, const float *__restrict__ src, int64_t lds,
+                      int src_vec, float *__restrict__ dst_hi, float *__restrict__ dst_lo,
+                      int64_t ldd) {
+    __shared__ float tile[TD][TD + 1];
+    const int64_t r0 = (int64_t)blockIdx.y * TD, c0 = (int64_t)blockIdx.x * TD;
+    const int t = threadIdx.x;
+    const int q = t & 15;         // float4 column within the tile
+    const int row = t >> 4;       // 0..15
 #pragma unroll
-    for (int r = ty; r < TT; r += TROWS) {
-        const int64_t m = m0 + r, k = k0 + tx;
-        if (m < M && k < K) tile[r][tx] = A[m * lda + k];
+    for (int i = 0; i < TD / 16; ++i) {
+        const int rr = row + 16 * i;
+        const int64_t r = r0 + rr, c = c0 + 4 * q;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r < R) {
+            const float *p = src + r * lds + c;
+            if (src_vec && c + 3 < Cc) {
+                const float4 x = *reinterpret_cast<const float4 *>(p);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (c + e < Cc) v[e] = p[e];
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tile[rr][4 * q + e] = v[e];
     }
     __syncthreads();
 #pragma unroll
-    for (int r = ty; r < TT; r += TROWS) {
-        const int64_t k = k0 + r, m = m0 + tx;
-        if (m < M && k < K) At[k * ldt + m] = tile[tx][r];
+    for (int i = 0; i < TD / 16; ++i) {
+        const int cc = row + 16 * i;          // destination row (source column)
+        const int64_t c = c0 + cc, r = r0 + 4 * q;
+        if (c >= Cc) continue;
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = tile[4 * q + e][cc];
+        float h[4], l[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (SPLIT) {
+                h[e] = tf32_rna(v[e]);
+                l[e] = tf32_rna(v[e] - h[e]);
+            } else {
+                h[e] = v[e];
+            }
+        }
+        float *ph = dst_hi + c * ldd + r;
+        float *pl = SPLIT ? dst_lo + c * ldd + r : nullptr;
+        if (r + 3 < R) {
+            *reinterpret_cast<float4 *>(ph) = make_float4(h[0], h[1], h[2], h[3]);
+            if (SPLIT) *reinterpret_cast<float4 *>(pl) = make_float4(l[0], l[1], l[2], l[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (r + e < R) {
+                    ph[e] = h[e];
+                    if (SPLIT) pl[e] = l[e];
+                }
+            }
+        }
     }
+}
+
+// hi/lo split of an R x Cc row-major matrix into two [R][ldo] arrays.
+__global__ void __launch_bounds__(256)
+split_rows_kernel(int64_t R, int64_t Cc, const float *__restrict__ X, int64_t ldx, int x_vec,
+                  float *__restrict__ hi, float *__restrict__ lo, int64_t ldo) {
+    const int64_t c4n = (Cc + 3) / 4;
+    for (int64_t r = blockIdx.y; r < R; r += gridDim.y) {
+        for (int64_t c4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c4 < c4n;
+             c4 += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t c = 4 * c4;
+            const float *p = X + r * ldx + c;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            const bool full = c + 3 < Cc;
+            if (x_vec && full) {
+                const float4 x = *reinterpret_cast<const float4 *>(p);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (c + e < Cc) v[e] = p[e];
+            }
+            float h[4], l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                h[e] = tf32_rna(v[e]);
+                l[e] = tf32_rna(v[e] - h[e]);
+            }
+            float *ph = hi + r * ldo + c, *pl = lo + r * ldo + c;
+            if (full) {
+                *reinterpret_cast<float4 *>(ph) = make_float4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<float4 *>(pl) = make_float4(l[0], l[1], l[2], l[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (c + e < Cc) {
+                        ph[e] = h[e];
+                        pl[e] = l[e];
+                    }
+            }
+        }
+    }
+}
+
+inline int vec_ok(const float *p, int64_t ld) {
+    return ((reinterpret_cast<uintptr_t>(p) & 15) == 0) && (ld % 4 == 0);
+}
+
+template <bool SPLIT>
+cudaError_t launch_tile(int64_t R, int64_t Cc, const float *src, int64_t lds, float *hi, float *lo,
+                        int64_t ldd, cudaStream_t stream) {
+    const int64_t gx = (Cc + TD - 1) / TD, gy = (R + TD - 1) / TD;
+    if (gy > 65535 || gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    if (gx == 0 || gy == 0) return cudaSuccess;
+    transpose_tile_kernel<SPLIT><<<dim3((unsigned)gx, (unsigned)gy), TTHREADS, 0, stream>>>(
+        R, Cc, src, lds, vec_ok(src, lds), hi, lo, ldd);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_transpose(int64_t M, int64_t K, const float *A, int64_t lda, float *At,
                              int64_t ldt, cudaStream_t stream) {
-    const int64_t gx = (K + TT - 1) / TT, gy = (M + TT - 1) / TT;
-    if (gy > 65535 || gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    transpose_kernel<<<dim3((unsigned)gx, (unsigned)gy), dim3(TT, TROWS), 0, stream>>>(M, K, A, lda,
-                                                                                      At, ldt);
+    return launch_tile<false>(M, K, A, lda, At, nullptr, ldt, stream);
+}
+
+cudaError_t launch_transpose_split(int64_t K, int64_t N, const float *B, int64_t ldb, float *hi,
+                                   float *lo, int64_t ldo, cudaStream_t stream) {
+    return launch_tile<true>(K, N, B, ldb, hi, lo, ldo, stream);
+}
+
+cudaError_t launch_split_rows(int64_t R, int64_t Cc, const float *X, int64_t ldx, float *hi,
+                              float *lo, int64_t ldo, cudaStream_t stream) {
+    const int64_t c4n = (Cc + 3) / 4;
+    const int64_t gx = (c4n + 255) / 256;
+    const dim3 grid((unsigned)(gx < 64 ? (gx > 0 ? gx : 1) : 64),
+                    (unsigned)(R < 65535 ? (R > 0 ? R : 1) : 65535));
+    split_rows_kernel<<<grid, 256, 0, stream>>>(R, Cc, X, ldx, vec_ok(X, ldx), hi, lo, ldo);
     return cudaGetLastError();
 }
 
