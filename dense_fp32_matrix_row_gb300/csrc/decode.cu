@@ -388,6 +388,202 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int
     cluster.sync();
 }
 
+// ---------------------------------------------------------------- tile variant (M >= 8)
+// The FFMA tile kernel's layout applied to the skinny product: a block owns
+// an MT x 256 tile of C; lane (ty, tx) of warp w owns rows ty*(MT/4) ..
+// +MT/4-1 and the eight columns w*64 + tx*4 + {0..3} and +32.  Per k it
+// loads its A rows with one shared load from the K-major A chunk and its
+// B columns with two 128-bit loads from the TMA-streamed B panel, then
+// forms an (MT/4) x 8 register outer product.  Every output belongs to one
+// thread, so there is no reduction across warps; registers stay near 64 and
+// shared memory small, so four blocks (16 warps) share an SM.
+constexpr int DT_COLS = 256, DT_WARPS = 4, DT_THREADS = DT_WARPS * 32;
+#ifndef DECODE_DT_TKB
+#define DECODE_DT_TKB 16
+#endif
+#ifndef DECODE_DT_STAGES
+#define DECODE_DT_STAGES 2
+#endif
+#ifndef DECODE_DT_KCH
+#define DECODE_DT_KCH 64
+#endif
+#ifndef DECODE_DT_MINB
+#define DECODE_DT_MINB 6
+#endif
+constexpr int DT_TKB = DECODE_DT_TKB, DT_STAGES = DECODE_DT_STAGES, DT_KCH = DECODE_DT_KCH;
+
+template <int MT>
+struct DtCfg {
+    static constexpr int TM = MT / 4;                                      // rows per lane
+    static constexpr size_t B_STAGE = (size_t)DT_TKB * DT_COLS;            // floats
+    static constexpr size_t RING = DT_STAGES * B_STAGE;
+    static constexpr size_t PART = (size_t)MT * DT_COLS;                  // aliases the ring
+    static constexpr size_t REGION0 = RING > PART ? RING : PART;
+    static constexpr size_t AS = (size_t)DT_KCH * MT;
+    static constexpr size_t BYTES = 128 + (REGION0 + AS) * 4 + DT_STAGES * 16;
+    static_assert(MT % 4 == 0 && MT >= 8, "four row groups of lanes");
+    static_assert(DT_KCH % DT_TKB == 0, "A chunks hold whole B panels");
+};
+
+template <int MT>
+__global__ void __launch_bounds__(DT_THREADS, DECODE_DT_MINB)
+decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int64_t K,
+                   float alpha, const float *__restrict__ A, int64_t lda, float beta,
+                   float *__restrict__ C, int64_t ldc, int64_t kslice, unsigned *err,
+                   uint64_t wait_ns) {
+    using L = DtCfg<MT>;
+    constexpr int TM = L::TM;
+    extern __shared__ unsigned char smem_raw[];
+    float *smem = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                            ~uintptr_t(127));
+    float *sB = smem;                      // [DT_STAGES][DT_TKB][DT_COLS]
+    float *part = smem;                    // [MT][DT_COLS], after the K loop
+    float *As = smem + L::REGION0;         // [DT_KCH][MT]
+    uint64_t *full = reinterpret_cast<uint64_t *>(As + L::AS);
+    unsigned *arrived = reinterpret_cast<unsigned *>(full + DT_STAGES);
+    int *issued = reinterpret_cast<int *>(arrived + DT_STAGES);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int ks = (int)cluster.num_blocks();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ty = lane >> 3, tx = lane & 7;
+    const int64_t n0 = (int64_t)blockIdx.y * DT_COLS;
+    const int64_t kbeg = (int64_t)rank * kslice;
+    const int64_t kend = (kbeg + kslice < K) ? kbeg + kslice : K;
+    const int nst = kend > kbeg ? (int)((kend - kbeg + DT_TKB - 1) / DT_TKB) : 0;
+    const int bcol = warp * 64 + tx * 4;
+
+    auto issue = [&](int st) {
+        const int s = st % DT_STAGES;
+        issued[s] = st;
+        const uint32_t fb = smem_u32(&full[s]);
+        mbar_arrive_expect_tx(fb, (uint32_t)(L::B_STAGE * 4));
+        tma_load_2d(smem_u32(sB + s * L::B_STAGE), &tmB, fb, (int32_t)n0,
+                    (int32_t)(kbeg + (int64_t)st * DT_TKB));
+    };
+    auto drain = [&]() {
+        for (int s = 0; s < DT_STAGES; ++s) {
+            const int st = *reinterpret_cast<volatile int *>(&issued[s]);
+            if (st >= 0) mbar_wait(smem_u32(&full[s]), (st / DT_STAGES) & 1, DRAIN_NS);
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < DT_STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            arrived[s] = 0;
+            issued[s] = -1;
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmB);
+        for (int st = 0; st < DT_STAGES && st < nst; ++st) issue(st);
+    }
+
+    float acc[TM][8];
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+    bool failed = false;
+
+    for (int st = 0; st < nst; ++st) {
+        const int64_t kc = kbeg + (int64_t)st * DT_TKB;
+        const int64_t chunk0 = kbeg + ((int64_t)st * DT_TKB) / DT_KCH * DT_KCH;
+        if (kc == chunk0) {
+            // Next chunk of A, K-major: As[k - chunk0][m]; rows past kend are zero.
+            __syncthreads();
+            const int64_t clen64 = (kend - chunk0) < DT_KCH ? (kend - chunk0) : DT_KCH;
+            const int clen = (int)clen64;
+            for (int idx = threadIdx.x; idx < DT_KCH * MT; idx += DT_THREADS) {
+                const int m = idx / DT_KCH, kl = idx - m * DT_KCH;
+                As[kl * MT + m] = (m < M && kl < clen) ? A[(int64_t)m * lda + chunk0 + kl] : 0.0f;
+            }
+            __syncthreads();
+        }
+        const int s = st % DT_STAGES;
+        if (!failed && !mbar_wait(smem_u32(&full[s]), (st / DT_STAGES) & 1, wait_ns)) {
+            failed = true;
+            if (lane == 0) {
+                record_error(err, kErrWaitTimeout);
+                drain();
+            }
+        }
+        if (failed) continue;
+        const float *bst = sB + s * L::B_STAGE + bcol;
+        const float *ast = As + (kc - chunk0) * MT + ty * TM;
+#pragma unroll
+        for (int r = 0; r < DT_TKB; ++r) {
+            float a[TM];
+            if constexpr (TM == 4) {
+                const float4 av = *reinterpret_cast<const float4 *>(ast + r * MT);
+                a[0] = av.x; a[1] = av.y; a[2] = av.z; a[3] = av.w;
+            } else if constexpr (TM == 2) {
+                const float2 av = *reinterpret_cast<const float2 *>(ast + r * MT);
+                a[0] = av.x; a[1] = av.y;
+            } else {
+#pragma unroll
+                for (int i = 0; i < TM; ++i) a[i] = ast[r * MT + i];
+            }
+            const float4 b0 = *reinterpret_cast<const float4 *>(bst + r * DT_COLS);
+            const float4 b1 = *reinterpret_cast<const float4 *>(bst + r * DT_COLS + 32);
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = (i & 1) ? 7 - jj : jj;
+                    acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
+                }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&arrived[s], 1u) == DT_WARPS - 1) {
+                arrived[s] = 0;
+                if (st + DT_STAGES < nst) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(st + DT_STAGES);
+                }
+            }
+        }
+    }
+
+    if (threadIdx.x == 0) drain();
+    const bool any_failed = __syncthreads_or(failed) != 0;
+    // Each thread's partial tile to shared memory (the ring is free now).
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        float *pr = part + (size_t)(ty * TM + i) * DT_COLS + bcol;
+        *reinterpret_cast<float4 *>(pr) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        *reinterpret_cast<float4 *>(pr + 32) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+    cluster.sync();
+    const int total = MT * DT_COLS;
+    const int per = (total + ks - 1) / ks;
+    const int obeg = rank * per;
+    const int oend = (obeg + per < total) ? obeg + per : total;
+    for (int o = obeg + threadIdx.x; o < oend; o += DT_THREADS) {
+        float pv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) pv[q] = q < ks ? cluster.map_shared_rank(part, q)[o] : 0.0f;
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum += pv[q];
+        const int m = o / DT_COLS;
+        const int64_t gn = n0 + (o - m * DT_COLS);
+        if (!any_failed && m < M && gn < N) {
+            float *p = C + (int64_t)m * ldc + gn;
+            const float v = alpha * sum;
+            *p = (beta != 0.0f) ? fmaf(beta, *p, v) : v;
+        }
+    }
+    cluster.sync();
+}
+
 // Cluster size: K split over ks blocks (<= 8, a portable cluster), chosen so
 // the grid fills whole waves of resident blocks as nearly as possible.
 inline int choose_ks(int64_t K, int64_t ncb, int slots) {
@@ -446,6 +642,9 @@ cudaError_t launch_tma(const GemmArgs &g) {
 #ifndef DECODE_DW
 #define DECODE_DW 8
 #endif
+#ifndef DECODE_TILE_MIN_M
+#define DECODE_TILE_MIN_M 5
+#endif
 #ifndef DECODE_STAGES
 #define DECODE_STAGES 3
 #endif
@@ -454,7 +653,46 @@ cudaError_t launch_tma(const GemmArgs &g) {
 #endif
 
 template <int MT>
+cudaError_t launch_tile(const GemmArgs &g) {
+    using L = DtCfg<MT>;
+    alignas(64) CUtensorMap tmB;
+    if (!encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, DT_COLS, DT_TKB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    auto kern = decode_tile_kernel<MT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DT_THREADS, L::BYTES);
+    if (e != cudaSuccess) return e;
+    const int64_t ncb = (g.N + DT_COLS - 1) / DT_COLS;
+    if (ncb > 65535) return cudaErrorInvalidConfiguration;
+    const int ks = choose_ks(g.K, ncb, (per_sm > 0 ? per_sm : 1) * (g.sm_count > 0 ? g.sm_count : 148));
+    int64_t kslice = (g.K + ks - 1) / ks;
+    kslice = (kslice + DT_TKB - 1) / DT_TKB * DT_TKB;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ks, (unsigned)ncb, 1);
+    cfg.blockDim = dim3(DT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.stream = g.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmB, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha, g.A,
+                              g.lda, g.beta, g.C, g.ldc, kslice, g.err, g.wait_ns);
+}
+
+template <int MT>
 cudaError_t launch_vec(const GemmArgs &g) {
+    if constexpr (MT >= 8) {
+        if (g.M >= DECODE_TILE_MIN_M && ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) &&
+            (g.ldb % 4 == 0))
+            return launch_tile<MT>(g);
+    }
     const bool vec = ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) && (g.ldb % 4 == 0);
     if (vec && g.M >= DECODE_TMA_MIN_M)
         return launch_tma<MT, DECODE_TNV, DECODE_DW, DECODE_STAGES>(g);
