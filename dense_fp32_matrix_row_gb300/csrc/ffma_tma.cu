@@ -76,6 +76,74 @@ __device__ __forceinline__ float comp(const float4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// acc += the stage's BK-deep outer products for this lane (see the layout above).
+template <class C>
+__device__ __forceinline__ void compute_stage(float (&acc)[C::TM][C::TN], const float *a_st,
+                                              const float *b_st) {
+    constexpr int TM = C::TM, TN = C::TN, BM = C::BM, BN = C::BN;
+#pragma unroll
+    for (int k = 0; k < C::BK; ++k) {
+        float4 a[TM / 4], b[TN / 4];
+#pragma unroll
+        for (int q = 0; q < TM / 4; ++q)
+            a[q] = *reinterpret_cast<const float4 *>(a_st + k * BM + 16 * q);
+#pragma unroll
+        for (int h = 0; h < TN / 4; ++h)
+            b[h] = *reinterpret_cast<const float4 *>(b_st + k * BN + 32 * h);
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const float av = comp(a[i / 4], i % 4);
+#pragma unroll
+            for (int jj = 0; jj < TN; ++jj) {
+                const int j = (i & 1) ? TN - 1 - jj : jj;
+                acc[i][j] = fmaf(av, comp(b[j / 4], j % 4), acc[i][j]);
+            }
+        }
+    }
+}
+
+// C = alpha*acc + beta*C for this lane's outputs of the tile at (m0, n0);
+// C is read only when beta != 0, stores are guarded at the matrix edge.
+template <class C>
+__device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int m0, int n0,
+                                           int arow, int bcol, int M, int N, float alpha,
+                                           float beta, float *__restrict__ Cm, int64_t ldc,
+                                           int c_vec4) {
+    constexpr int TM = C::TM, TN = C::TN;
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        const int gm = m0 + arow + 16 * (i / 4) + (i % 4);
+        if (gm >= M) continue;
+        float *crow = Cm + (int64_t)gm * ldc;
+#pragma unroll
+        for (int h = 0; h < TN / 4; ++h) {
+            const int gn = n0 + bcol + 32 * h;
+            float v[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = alpha * acc[i][4 * h + e];
+            if (c_vec4 && gn + 3 < N) {
+                float4 *p = reinterpret_cast<float4 *>(crow + gn);
+                if (beta != 0.0f) {
+                    const float4 o = *p;
+                    v[0] = fmaf(beta, o.x, v[0]);
+                    v[1] = fmaf(beta, o.y, v[1]);
+                    v[2] = fmaf(beta, o.z, v[2]);
+                    v[3] = fmaf(beta, o.w, v[3]);
+                }
+                *p = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (gn + e < N) {
+                        float *p = crow + gn + e;
+                        *p = (beta != 0.0f) ? fmaf(beta, *p, v[e]) : v[e];
+                    }
+                }
+            }
+        }
+    }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmB,
@@ -148,27 +216,7 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
             }
             return;
         }
-        const float *a_st = sA + s * C::A_STAGE + arow;
-        const float *b_st = sB + s * C::B_STAGE + bcol;
-#pragma unroll
-        for (int k = 0; k < BK; ++k) {
-            float4 a[TM / 4], b[TN / 4];
-#pragma unroll
-            for (int q = 0; q < TM / 4; ++q)
-                a[q] = *reinterpret_cast<const float4 *>(a_st + k * BM + 16 * q);
-#pragma unroll
-            for (int h = 0; h < TN / 4; ++h)
-                b[h] = *reinterpret_cast<const float4 *>(b_st + k * BN + 32 * h);
-#pragma unroll
-            for (int i = 0; i < TM; ++i) {
-                const float av = comp(a[i / 4], i % 4);
-#pragma unroll
-                for (int jj = 0; jj < TN; ++jj) {
-                    const int j = (i & 1) ? TN - 1 - jj : jj;
-                    acc[i][j] = fmaf(av, comp(b[j / 4], j % 4), acc[i][j]);
-                }
-            }
-        }
+        compute_stage<C>(acc, sA + s * C::A_STAGE + arow, sB + s * C::B_STAGE + bcol);
         // Release the stage; the last warp to do so refills it STAGES k-tiles ahead.
         __syncwarp();
         if (lane == 0) {
@@ -184,38 +232,7 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
     }
 
     // ---------------------------------------------------------------- epilogue
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        const int gm = m0 + arow + 16 * (i / 4) + (i % 4);
-        if (gm >= M) continue;
-        float *crow = Cm + (int64_t)gm * ldc;
-#pragma unroll
-        for (int h = 0; h < TN / 4; ++h) {
-            const int gn = n0 + bcol + 32 * h;
-            float v[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = alpha * acc[i][4 * h + e];
-            if (c_vec4 && gn + 3 < N) {
-                float4 *p = reinterpret_cast<float4 *>(crow + gn);
-                if (beta != 0.0f) {
-                    const float4 o = *p;
-                    v[0] = fmaf(beta, o.x, v[0]);
-                    v[1] = fmaf(beta, o.y, v[1]);
-                    v[2] = fmaf(beta, o.z, v[2]);
-                    v[3] = fmaf(beta, o.w, v[3]);
-                }
-                *p = make_float4(v[0], v[1], v[2], v[3]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if (gn + e < N) {
-                        float *p = crow + gn + e;
-                        *p = (beta != 0.0f) ? fmaf(beta, *p, v[e]) : v[e];
-                    }
-                }
-            }
-        }
-    }
+    store_tile<C>(acc, m0, n0, arow, bcol, M, N, alpha, beta, Cm, ldc, c_vec4);
 }
 
 template <class C>

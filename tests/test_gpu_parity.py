@@ -329,3 +329,20 @@ def test_workload_8192_3xtf32_sampled_rows():
     _, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"], tensor_cores=True,
                             rows=_sample_rows(w["M"]))
     assert chosen == TF
+
+
+# ---------------------------------------------------------------- large ragged shapes
+# More tiles than resident blocks, ragged edges in M and N, K not a multiple of
+# the 32-deep k-tile; every output compared.
+@pytest.mark.parametrize("M,N,K,beta", [(2300, 2350, 700, 0.7), (2431, 2305, 1001, 0.0)])
+def test_large_ragged_full_compare(M, N, K, beta):
+    A, B, C0 = make_inputs(M, N, K, "uniform", seed=M + K, beta=beta)
+    ldb = (N + 3) // 4 * 4        # B must be TMA-readable; N itself stays ragged
+    _, chosen = run_checked(sg, A, B, C0, 1.5, beta, lds=(K, ldb, N))
+    assert chosen == TMA
+
+
+def test_large_small_integers_exact():
+    A, B, C0 = make_inputs(2200, 2400, 300, "int", seed=9, beta=-1.0)
+    _, chosen = run_checked(sg, A, B, C0, 2.0, -1.0, exact=True)
+    assert chosen == TMA
