@@ -435,7 +435,7 @@ def run_ours(args, world, rank, local):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 FLOP x "
                                     f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz ({peaks['_source']} max clock)",
-                     "kernel": ("transpose_kernel + ffma_tma_kernel, timed together as one sgemm() "
+                     "kernel": ("transpose_tile_kernel<0> + ffma_tma_kernel, timed together as one sgemm() "
                                 "call; traffic is ffma_tma_kernel's alone"
                                 if kid == sg.KERNEL_FFMA_TMA else sg.KERNEL_NAMES.get(kid, str(kid))),
                      "per_call_ms": per_launch_ms},
