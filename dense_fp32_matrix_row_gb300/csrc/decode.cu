@@ -21,6 +21,7 @@
 //    cluster owns and applies C = alpha*sum + beta*C (C read only if beta != 0).
 #include <cooperative_groups.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "common.cuh"
@@ -388,15 +389,40 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int
     cluster.sync();
 }
 
-// ---------------------------------------------------------------- tile variant (M >= 8)
+// acc[j] += a * b[j] for j < 8, as packed two-lane FP32 FMAs (each lane a
+// fused multiply-add rounded once, exactly as fmaf); `rev` walks the pairs
+// backwards (alternating rows keep operands of neighbouring FMAs apart).
+__device__ __forceinline__ void fma_row8(float (&acc)[8], float a, const float (&b)[8], bool rev) {
+    const float2 a2 = make_float2(a, a);
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+        const int q = rev ? 3 - qq : qq;
+        const float2 d = __ffma2_rn(a2, make_float2(b[2 * q], b[2 * q + 1]),
+                                    make_float2(acc[2 * q], acc[2 * q + 1]));
+        acc[2 * q] = d.x;
+        acc[2 * q + 1] = d.y;
+    }
+}
+
+// ---------------------------------------------------------------- tile variant (M >= 5)
 // The FFMA tile kernel's layout applied to the skinny product: a block owns
 // an MT x 256 tile of C; lane (ty, tx) of warp w owns rows ty*(MT/4) ..
-// +MT/4-1 and the eight columns w*64 + tx*4 + {0..3} and +32.  Per k it
-// loads its A rows with one shared load from the K-major A chunk and its
-// B columns with two 128-bit loads from the TMA-streamed B panel, then
-// forms an (MT/4) x 8 register outer product.  Every output belongs to one
-// thread, so there is no reduction across warps; registers stay near 64 and
-// shared memory small, so four blocks (16 warps) share an SM.
+// +MT/4-1 and the eight columns w*64 + tx*4 + {0..3} and +32, an (MT/4) x 8
+// register outer product per k.  Every output belongs to one thread, so
+// there is no reduction across warps, and at 80 registers six blocks share
+// an SM.
+//
+// Each stage of the TMA ring carries both operands of DT_TKB k-steps: the
+// DT_TKB x 256 panel of B and the MT x DT_TKB panel of A (row-major, rows
+// past M zero-filled by the copy).  A lane reads its A rows four k at a time
+// with one 128-bit load per row, so the K loop has no block barrier and no
+// global load of its own: every wait is on a copy that was issued
+// DT_STAGES - 1 panels earlier.  Requires A and B 16-byte aligned with
+// lda % 4 == 0 and ldb % 4 == 0.
+//
+// K is split over the blocks of a cluster of up to DT_KSMAX (16 needs the
+// non-portable cluster size); the launcher takes the largest split whose
+// clusters all fit on the GPU at once.
 constexpr int DT_COLS = 256, DT_WARPS = 4, DT_THREADS = DT_WARPS * 32;
 #ifndef DECODE_DT_TKB
 #define DECODE_DT_TKB 16
@@ -404,42 +430,43 @@ constexpr int DT_COLS = 256, DT_WARPS = 4, DT_THREADS = DT_WARPS * 32;
 #ifndef DECODE_DT_STAGES
 #define DECODE_DT_STAGES 2
 #endif
-#ifndef DECODE_DT_KCH
-#define DECODE_DT_KCH 64
-#endif
 #ifndef DECODE_DT_MINB
 #define DECODE_DT_MINB 6
 #endif
-constexpr int DT_TKB = DECODE_DT_TKB, DT_STAGES = DECODE_DT_STAGES, DT_KCH = DECODE_DT_KCH;
+#ifndef DECODE_DT_KSMAX
+#define DECODE_DT_KSMAX 16
+#endif
+constexpr int DT_TKB = DECODE_DT_TKB, DT_STAGES = DECODE_DT_STAGES, DT_KSMAX = DECODE_DT_KSMAX;
 
 template <int MT>
 struct DtCfg {
     static constexpr int TM = MT / 4;                                      // rows per lane
-    static constexpr size_t B_STAGE = (size_t)DT_TKB * DT_COLS;            // floats
-    static constexpr size_t RING = DT_STAGES * B_STAGE;
+    static constexpr size_t B_PANEL = (size_t)DT_TKB * DT_COLS;            // floats, [k][n]
+    static constexpr size_t A_PANEL = (size_t)MT * DT_TKB;                 // floats, [m][k]
+    static constexpr size_t STAGE = B_PANEL + A_PANEL;
+    static constexpr size_t RING = DT_STAGES * STAGE;
     static constexpr size_t PART = (size_t)MT * DT_COLS;                  // aliases the ring
     static constexpr size_t REGION0 = RING > PART ? RING : PART;
-    static constexpr size_t AS = (size_t)DT_KCH * MT;
-    static constexpr size_t BYTES = 128 + (REGION0 + AS) * 4 + DT_STAGES * 16;
+    static constexpr size_t BYTES = 128 + REGION0 * 4 + DT_STAGES * 16;
     static_assert(MT % 4 == 0 && MT >= 8, "four row groups of lanes");
-    static_assert(DT_KCH % DT_TKB == 0, "A chunks hold whole B panels");
+    static_assert(DT_TKB % 4 == 0, "A rows are read four k at a time");
+    static_assert((STAGE * 4) % 128 == 0, "stage offsets stay 128-byte aligned");
+    static_assert(DT_KSMAX == 8 || DT_KSMAX == 16, "cluster size");
 };
 
 template <int MT>
 __global__ void __launch_bounds__(DT_THREADS, DECODE_DT_MINB)
-decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int64_t K,
-                   float alpha, const float *__restrict__ A, int64_t lda, float beta,
-                   float *__restrict__ C, int64_t ldc, int64_t kslice, unsigned *err,
-                   uint64_t wait_ns) {
+decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
+                   int M, int64_t N, int64_t K, float alpha, float beta, float *__restrict__ C,
+                   int64_t ldc, int64_t kslice, unsigned *err, uint64_t wait_ns) {
     using L = DtCfg<MT>;
     constexpr int TM = L::TM;
     extern __shared__ unsigned char smem_raw[];
     float *smem = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                             ~uintptr_t(127));
-    float *sB = smem;                      // [DT_STAGES][DT_TKB][DT_COLS]
+    float *ring = smem;                    // [DT_STAGES][B panel | A panel]
     float *part = smem;                    // [MT][DT_COLS], after the K loop
-    float *As = smem + L::REGION0;         // [DT_KCH][MT]
-    uint64_t *full = reinterpret_cast<uint64_t *>(As + L::AS);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::REGION0);
     unsigned *arrived = reinterpret_cast<unsigned *>(full + DT_STAGES);
     int *issued = reinterpret_cast<int *>(arrived + DT_STAGES);
 
@@ -458,9 +485,11 @@ decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, in
         const int s = st % DT_STAGES;
         issued[s] = st;
         const uint32_t fb = smem_u32(&full[s]);
-        mbar_arrive_expect_tx(fb, (uint32_t)(L::B_STAGE * 4));
-        tma_load_2d(smem_u32(sB + s * L::B_STAGE), &tmB, fb, (int32_t)n0,
-                    (int32_t)(kbeg + (int64_t)st * DT_TKB));
+        const int32_t kc = (int32_t)(kbeg + (int64_t)st * DT_TKB);
+        float *stg = ring + s * L::STAGE;
+        mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE * 4));
+        tma_load_2d(smem_u32(stg), &tmB, fb, (int32_t)n0, kc);
+        tma_load_2d(smem_u32(stg + L::B_PANEL), &tmA, fb, kc, 0);
     };
     auto drain = [&]() {
         for (int s = 0; s < DT_STAGES; ++s) {
@@ -480,6 +509,7 @@ decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, in
     __syncthreads();
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmA);
         for (int st = 0; st < DT_STAGES && st < nst; ++st) issue(st);
     }
 
@@ -491,53 +521,36 @@ decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, in
     bool failed = false;
 
     for (int st = 0; st < nst; ++st) {
-        const int64_t kc = kbeg + (int64_t)st * DT_TKB;
-        const int64_t chunk0 = kbeg + ((int64_t)st * DT_TKB) / DT_KCH * DT_KCH;
-        if (kc == chunk0) {
-            // Next chunk of A, K-major: As[k - chunk0][m]; rows past kend are zero.
-            __syncthreads();
-            const int64_t clen64 = (kend - chunk0) < DT_KCH ? (kend - chunk0) : DT_KCH;
-            const int clen = (int)clen64;
-            for (int idx = threadIdx.x; idx < DT_KCH * MT; idx += DT_THREADS) {
-                const int m = idx / DT_KCH, kl = idx - m * DT_KCH;
-                As[kl * MT + m] = (m < M && kl < clen) ? A[(int64_t)m * lda + chunk0 + kl] : 0.0f;
-            }
-            __syncthreads();
-        }
         const int s = st % DT_STAGES;
-        if (!failed && !mbar_wait(smem_u32(&full[s]), (st / DT_STAGES) & 1, wait_ns)) {
+        if (!mbar_wait(smem_u32(&full[s]), (st / DT_STAGES) & 1, wait_ns)) {
             failed = true;
             if (lane == 0) {
                 record_error(err, kErrWaitTimeout);
                 drain();
             }
+            break;
         }
-        if (failed) continue;
-        const float *bst = sB + s * L::B_STAGE + bcol;
-        const float *ast = As + (kc - chunk0) * MT + ty * TM;
+        const float *stg = ring + s * L::STAGE;
+        const float *bst = stg + bcol;
+        const float *ast = stg + L::B_PANEL + (size_t)ty * TM * DT_TKB;
 #pragma unroll
-        for (int r = 0; r < DT_TKB; ++r) {
-            float a[TM];
-            if constexpr (TM == 4) {
-                const float4 av = *reinterpret_cast<const float4 *>(ast + r * MT);
-                a[0] = av.x; a[1] = av.y; a[2] = av.z; a[3] = av.w;
-            } else if constexpr (TM == 2) {
-                const float2 av = *reinterpret_cast<const float2 *>(ast + r * MT);
-                a[0] = av.x; a[1] = av.y;
-            } else {
-#pragma unroll
-                for (int i = 0; i < TM; ++i) a[i] = ast[r * MT + i];
-            }
-            const float4 b0 = *reinterpret_cast<const float4 *>(bst + r * DT_COLS);
-            const float4 b1 = *reinterpret_cast<const float4 *>(bst + r * DT_COLS + 32);
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        for (int r4 = 0; r4 < DT_TKB; r4 += 4) {
+            float4 av[TM];
 #pragma unroll
             for (int i = 0; i < TM; ++i)
+                av[i] = *reinterpret_cast<const float4 *>(ast + i * DT_TKB + r4);
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int j = (i & 1) ? 7 - jj : jj;
-                    acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
+            for (int rr = 0; rr < 4; ++rr) {
+                const int r = r4 + rr;
+                const float4 b0 = *reinterpret_cast<const float4 *>(bst + r * DT_COLS);
+                const float4 b1 = *reinterpret_cast<const float4 *>(bst + r * DT_COLS + 32);
+                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const float a = rr == 0 ? av[i].x : rr == 1 ? av[i].y : rr == 2 ? av[i].z : av[i].w;
+                    fma_row8(acc[i], a, bv, i & 1);
                 }
+            }
         }
         __syncwarp();
         if (lane == 0) {
@@ -552,6 +565,8 @@ decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, in
         }
     }
 
+    // After a time-out the warp that saw it waited for every copy in flight;
+    // the others may have stopped at an earlier stage, so wait for all here.
     if (threadIdx.x == 0) drain();
     const bool any_failed = __syncthreads_or(failed) != 0;
     // Each thread's partial tile to shared memory (the ring is free now).
@@ -567,18 +582,225 @@ decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, in
     const int obeg = rank * per;
     const int oend = (obeg + per < total) ? obeg + per : total;
     for (int o = obeg + threadIdx.x; o < oend; o += DT_THREADS) {
-        float pv[8];
+        // independent remote loads first, then the sum in rank order
+        float pv[DT_KSMAX];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) pv[q] = q < ks ? cluster.map_shared_rank(part, q)[o] : 0.0f;
-        float sum = 0.0f;
+        for (int q = 0; q < DT_KSMAX; ++q) pv[q] = q < ks ? cluster.map_shared_rank(part, q)[o] : 0.0f;
+        float sum = pv[0];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) sum += pv[q];
+        for (int q = 1; q < DT_KSMAX; ++q)
+            if (q < ks) sum += pv[q];
         const int m = o / DT_COLS;
         const int64_t gn = n0 + (o - m * DT_COLS);
         if (!any_failed && m < M && gn < N) {
             float *p = C + (int64_t)m * ldc + gn;
             const float v = alpha * sum;
             *p = (beta != 0.0f) ? fmaf(beta, *p, v) : v;
+        }
+    }
+    cluster.sync();
+}
+
+// ---------------------------------------------------------------- outer-product variant (M >= 5)
+// The four warps of a block split the block's MT x 256 tile into RG row
+// groups and every stage's k-steps into KG = 4/RG interleaved k groups.  A
+// lane owns the MT/RG rows of its row group and eight columns (lane*4 +
+// {0..3} and 128 + lane*4 + {0..3}): an (MT/RG) x 8 outer product per k.
+// Per k a lane loads 8 floats of B (two 128-bit loads) and MT/RG broadcast
+// floats of A, so shared memory delivers (MT/RG + 8) floats per lane for
+// 8*MT/RG FFMAs: 0.25 wavefronts per FFMA at MT/RG = 8, against 0.375 for
+// the tile layout above (4 rows per lane).  At M = 16 a byte of B carries
+// four FFMAs, so streaming B at the copy rate needs the FMA pipe about two
+// thirds busy, and the shared-memory pipe is the first to saturate.
+//
+// Stages carry both operands (B panel [k][n], A panel [m][k]) as in the tile
+// variant.  After the K loop the k groups' partial tiles are summed in a
+// fixed order in shared memory, then across the cluster.
+constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32, DO_TKB = 16;
+#ifndef DECODE_DO_STAGES
+#define DECODE_DO_STAGES 2
+#endif
+#ifndef DECODE_DO_MINB
+#define DECODE_DO_MINB 4
+#endif
+constexpr int DO_STAGES = DECODE_DO_STAGES;
+constexpr int DO_KSMAX = 16;   // cluster size limit (16 is non-portable)
+
+template <int MT, int RG>
+struct DoCfg {
+    static constexpr int KG = DO_WARPS / RG;                               // k groups
+    static constexpr int MTL = MT / RG;                                    // rows per lane
+    static constexpr int RPW = DO_TKB / KG;                                // k-steps per warp per stage
+    static constexpr size_t B_PANEL = (size_t)DO_TKB * DO_COLS;            // floats, [k][n]
+    static constexpr size_t A_PANEL = (size_t)MT * DO_TKB;                 // floats, [m][k]
+    static constexpr size_t STAGE = B_PANEL + A_PANEL;
+    static constexpr size_t RING = DO_STAGES * STAGE;
+    static constexpr size_t RED = (size_t)KG * MT * DO_COLS;              // aliases the ring
+    static constexpr size_t REGION0 = RING > RED ? RING : RED;
+    static constexpr size_t BYTES = 128 + REGION0 * 4 + DO_STAGES * 16;
+    static_assert(DO_WARPS % RG == 0 && MT % RG == 0 && DO_TKB % KG == 0, "warp split");
+    static_assert((STAGE * 4) % 128 == 0, "stage offsets stay 128-byte aligned");
+    static_assert((MT * DO_COLS) % (4 * DO_THREADS) == 0, "whole float4 sweeps in the group sum");
+};
+
+template <int MT, int RG>
+__global__ void __launch_bounds__(DO_THREADS, DECODE_DO_MINB)
+decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
+                    int M, int64_t N, int64_t K, float alpha, float beta, float *__restrict__ C,
+                    int64_t ldc, int64_t kslice, unsigned *err, uint64_t wait_ns) {
+    using L = DoCfg<MT, RG>;
+    constexpr int KG = L::KG, MTL = L::MTL;
+    extern __shared__ unsigned char smem_raw[];
+    float *smem = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                            ~uintptr_t(127));
+    float *ring = smem;                    // [DO_STAGES][B panel | A panel]
+    float *red = smem;                     // [KG][MT][DO_COLS], after the K loop
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::REGION0);
+    unsigned *arrived = reinterpret_cast<unsigned *>(full + DO_STAGES);
+    int *issued = reinterpret_cast<int *>(arrived + DO_STAGES);
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int ks = (int)cluster.num_blocks();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rg = warp / KG, kg = warp % KG;
+    const int64_t n0 = (int64_t)blockIdx.y * DO_COLS;
+    const int64_t kbeg = (int64_t)rank * kslice;
+    const int64_t kend = (kbeg + kslice < K) ? kbeg + kslice : K;
+    const int nst = kend > kbeg ? (int)((kend - kbeg + DO_TKB - 1) / DO_TKB) : 0;
+
+    auto issue = [&](int st) {
+        const int s = st % DO_STAGES;
+        issued[s] = st;
+        const uint32_t fb = smem_u32(&full[s]);
+        const int32_t kc = (int32_t)(kbeg + (int64_t)st * DO_TKB);
+        float *stg = ring + s * L::STAGE;
+        mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE * 4));
+        tma_load_2d(smem_u32(stg), &tmB, fb, (int32_t)n0, kc);
+        tma_load_2d(smem_u32(stg + L::B_PANEL), &tmA, fb, kc, 0);
+    };
+    auto drain = [&]() {
+        for (int s = 0; s < DO_STAGES; ++s) {
+            const int st = *reinterpret_cast<volatile int *>(&issued[s]);
+            if (st >= 0) mbar_wait(smem_u32(&full[s]), (st / DO_STAGES) & 1, DRAIN_NS);
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < DO_STAGES; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            arrived[s] = 0;
+            issued[s] = -1;
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmA);
+        for (int st = 0; st < DO_STAGES && st < nst; ++st) issue(st);
+    }
+
+    float acc[MTL][8];
+#pragma unroll
+    for (int m = 0; m < MTL; ++m)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[m][j] = 0.0f;
+    bool failed = false;
+
+    for (int st = 0; st < nst; ++st) {
+        const int s = st % DO_STAGES;
+        if (!mbar_wait(smem_u32(&full[s]), (st / DO_STAGES) & 1, wait_ns)) {
+            failed = true;
+            if (lane == 0) {
+                record_error(err, kErrWaitTimeout);
+                drain();
+            }
+            break;
+        }
+        const float *stg = ring + s * L::STAGE;
+        const float *bst = stg + lane * 4;
+        const float *ast = stg + L::B_PANEL + (size_t)rg * MTL * DO_TKB;
+#pragma unroll
+        for (int rr = 0; rr < L::RPW; ++rr) {
+            const int r = kg + KG * rr;
+            const float4 b0 = *reinterpret_cast<const float4 *>(bst + r * DO_COLS);
+            const float4 b1 = *reinterpret_cast<const float4 *>(bst + r * DO_COLS + 128);
+            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int m = 0; m < MTL; ++m) fma_row8(acc[m], ast[m * DO_TKB + r], bv, m & 1);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&arrived[s], 1u) == DO_WARPS - 1) {
+                arrived[s] = 0;
+                if (st + DO_STAGES < nst) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(st + DO_STAGES);
+                }
+            }
+        }
+    }
+
+    if (threadIdx.x == 0) drain();
+    const bool any_failed = __syncthreads_or(failed) != 0;
+    // k-group partials to shared memory (the ring is free now), then their
+    // sum in k-group order into group 0's slot.
+#pragma unroll
+    for (int m = 0; m < MTL; ++m) {
+        float *pr = red + ((size_t)kg * MT + rg * MTL + m) * DO_COLS + lane * 4;
+        *reinterpret_cast<float4 *>(pr) = make_float4(acc[m][0], acc[m][1], acc[m][2], acc[m][3]);
+        *reinterpret_cast<float4 *>(pr + 128) = make_float4(acc[m][4], acc[m][5], acc[m][6], acc[m][7]);
+    }
+    __syncthreads();
+    constexpr int TOTAL4 = MT * DO_COLS / 4;
+    if constexpr (KG > 1) {
+#pragma unroll
+        for (int it = 0; it < TOTAL4 / DO_THREADS; ++it) {
+            const int o4 = threadIdx.x + it * DO_THREADS;
+            float4 v = reinterpret_cast<const float4 *>(red)[o4];
+#pragma unroll
+            for (int w = 1; w < KG; ++w) {
+                const float4 u = reinterpret_cast<const float4 *>(red + (size_t)w * MT * DO_COLS)[o4];
+                v.x += u.x; v.y += u.y; v.z += u.z; v.w += u.w;
+            }
+            reinterpret_cast<float4 *>(red)[o4] = v;
+        }
+    }
+    cluster.sync();
+    // Block `rank` finishes float4 groups [rank*per4, (rank+1)*per4) of the
+    // cluster's MT x 256 tile: the ks partials in rank order, then alpha/beta.
+    const int per4 = (TOTAL4 + ks - 1) / ks;
+    const int obeg = rank * per4;
+    const int oend = (obeg + per4 < TOTAL4) ? obeg + per4 : TOTAL4;
+    for (int o4 = obeg + threadIdx.x; o4 < oend; o4 += DO_THREADS) {
+        // four remote loads in flight at a time; the sum stays in rank order
+        float4 sum = reinterpret_cast<const float4 *>(cluster.map_shared_rank(red, 0))[o4];
+        for (int q0 = 1; q0 < ks; q0 += 4) {
+            float4 pv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (q0 + u < ks)
+                    pv[u] = reinterpret_cast<const float4 *>(cluster.map_shared_rank(red, q0 + u))[o4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (q0 + u < ks) {
+                    sum.x += pv[u].x; sum.y += pv[u].y; sum.z += pv[u].z; sum.w += pv[u].w;
+                }
+        }
+        const int m = (4 * o4) / DO_COLS;
+        const int64_t gn = n0 + (4 * o4 - m * DO_COLS);
+        if (!any_failed && m < M) {
+            const float sv[4] = {sum.x, sum.y, sum.z, sum.w};
+            float *p = C + (int64_t)m * ldc + gn;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (gn + e < N) {
+                    const float v = alpha * sv[e];
+                    p[e] = (beta != 0.0f) ? fmaf(beta, p[e], v) : v;
+                }
+            }
         }
     }
     cluster.sync();
@@ -642,6 +864,9 @@ cudaError_t launch_tma(const GemmArgs &g) {
 #ifndef DECODE_DW
 #define DECODE_DW 8
 #endif
+#ifndef DECODE_M16
+#define DECODE_M16 1     // 1: outer-product kernel with two row groups, 0: tile kernel
+#endif
 #ifndef DECODE_TILE_MIN_M
 #define DECODE_TILE_MIN_M 5
 #endif
@@ -652,29 +877,83 @@ cudaError_t launch_tma(const GemmArgs &g) {
 #define DECODE_TMA_MIN_M 1
 #endif
 
-template <int MT>
-cudaError_t launch_tile(const GemmArgs &g) {
-    using L = DtCfg<MT>;
-    alignas(64) CUtensorMap tmB;
-    if (!encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, DT_COLS, DT_TKB, CU_TENSOR_MAP_SWIZZLE_NONE))
+// Largest number of clusters of `ks` blocks of `kern` the GPU holds at once,
+// cached per device and cluster size (0: this cluster size cannot launch).
+template <typename Kern>
+int max_clusters(Kern kern, int ks, cudaLaunchConfig_t cfg, std::atomic<int> (&cache)[64][17]) {
+    int dev = 0;
+    if (ks < 1 || ks > 16 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    const int hit = cache[dev][ks].load(std::memory_order_relaxed);
+    if (hit > 0) return hit - 1;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)ks, 1, 1);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    cache[dev][ks].store(n + 1, std::memory_order_relaxed);
+    return n;
+}
+
+// Cluster size for a K split over the blocks of a cluster: among sizes
+// 1..ksmax that leave each block at least `min_k` k-steps, the one whose
+// grid (ncb clusters) fills its waves best; within 2% of the best, the
+// largest (more blocks in flight hide more memory latency).
+template <typename Kern>
+int choose_cluster(Kern kern, int64_t K, int64_t ncb, int ksmax, int min_k, const cudaLaunchConfig_t &cfg,
+                   std::atomic<int> (&cache)[64][17]) {
+    int ks = 1;
+    double best_eff = -1.0;
+    for (int c = 1; c <= ksmax; ++c) {
+        if (c > 1 && K / c < min_k) break;
+        const int nclu = max_clusters(kern, c, cfg, cache);
+        if (nclu <= 0) continue;
+        const double waves = (double)ncb / nclu;
+        const double eff = waves / std::ceil(waves);
+        if (eff > best_eff + 0.02 || (eff > best_eff - 0.02 && c > ks)) {
+            ks = c;
+            best_eff = eff > best_eff ? eff : best_eff;
+        }
+    }
+    return ks;
+}
+
+template <int MT, int RG>
+cudaError_t launch_outer(const GemmArgs &g) {
+    using L = DoCfg<MT, RG>;
+    static std::atomic<int> cache[64][17];
+    alignas(64) CUtensorMap tmB, tmA;
+    if (!encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, DO_COLS, DO_TKB, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kern = decode_tile_kernel<MT>;
+    if (!encode_tma_2d(g.encode, &tmA, g.A, g.K, g.M, g.lda, DO_TKB, MT, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    auto kern = decode_outer_kernel<MT, RG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, DT_THREADS, L::BYTES);
-    if (e != cudaSuccess) return e;
-    const int64_t ncb = (g.N + DT_COLS - 1) / DT_COLS;
+    int ksmax = 8;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)
+        ksmax = DO_KSMAX;
+    else
+        (void)cudaGetLastError();
+    const int64_t ncb = (g.N + DO_COLS - 1) / DO_COLS;
     if (ncb > 65535) return cudaErrorInvalidConfiguration;
-    const int ks = choose_ks(g.K, ncb, (per_sm > 0 ? per_sm : 1) * (g.sm_count > 0 ? g.sm_count : 148));
-    int64_t kslice = (g.K + ks - 1) / ks;
-    kslice = (kslice + DT_TKB - 1) / DT_TKB * DT_TKB;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ks, (unsigned)ncb, 1);
-    cfg.blockDim = dim3(DT_THREADS, 1, 1);
+    cfg.blockDim = dim3(DO_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::BYTES;
     cfg.stream = g.stream;
+    const int ks = choose_cluster(kern, g.K, ncb, ksmax, DO_TKB, cfg, cache);
+    int64_t kslice = (g.K + ks - 1) / ks;
+    kslice = (kslice + DO_TKB - 1) / DO_TKB * DO_TKB;
+
+    cfg.gridDim = dim3((unsigned)ks, (unsigned)ncb, 1);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)ks;
@@ -682,16 +961,64 @@ cudaError_t launch_tile(const GemmArgs &g) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmB, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha, g.A,
-                              g.lda, g.beta, g.C, g.ldc, kslice, g.err, g.wait_ns);
+    return cudaLaunchKernelEx(&cfg, kern, tmB, tmA, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha,
+                              g.beta, g.C, g.ldc, kslice, g.err, g.wait_ns);
+}
+
+template <int MT>
+cudaError_t launch_tile(const GemmArgs &g) {
+    using L = DtCfg<MT>;
+    alignas(64) CUtensorMap tmB, tmA;
+    if (!encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, DT_COLS, DT_TKB, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    if (!encode_tma_2d(g.encode, &tmA, g.A, g.K, g.M, g.lda, DT_TKB, MT, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    auto kern = decode_tile_kernel<MT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
+    if (e != cudaSuccess) return e;
+    int ksmax = 8;
+    if (DT_KSMAX > 8) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)
+            ksmax = DT_KSMAX;
+        else
+            (void)cudaGetLastError();
+    }
+    const int64_t ncb = (g.N + DT_COLS - 1) / DT_COLS;
+    if (ncb > 65535) return cudaErrorInvalidConfiguration;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(DT_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.stream = g.stream;
+    static std::atomic<int> cache[64][17];
+    const int ks = choose_cluster(kern, g.K, ncb, ksmax, DT_TKB, cfg, cache);
+    int64_t kslice = (g.K + ks - 1) / ks;
+    kslice = (kslice + DT_TKB - 1) / DT_TKB * DT_TKB;
+
+    cfg.gridDim = dim3((unsigned)ks, (unsigned)ncb, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmB, tmA, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha,
+                              g.beta, g.C, g.ldc, kslice, g.err, g.wait_ns);
 }
 
 template <int MT>
 cudaError_t launch_vec(const GemmArgs &g) {
     if constexpr (MT >= 8) {
         if (g.M >= DECODE_TILE_MIN_M && ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) &&
-            (g.ldb % 4 == 0))
-            return launch_tile<MT>(g);
+            (g.ldb % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.A) & 15) == 0) && (g.lda % 4 == 0)) {
+            if constexpr (MT <= 8)
+                return launch_outer<MT, 1>(g);
+            else if constexpr (DECODE_M16 == 1)
+                return launch_outer<MT, 2>(g);
+            else
+                return launch_tile<MT>(g);
+        }
     }
     const bool vec = ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) && (g.ldb % 4 == 0);
     if (vec && g.M >= DECODE_TMA_MIN_M)

@@ -33,6 +33,9 @@
 //                                 and columns wn*8*TN + 32*(j/4) + 4*tx + j%4   (j < TN).
 #include "common.cuh"
 
+#ifndef FFMA_PACKED
+#define FFMA_PACKED 1
+#endif
 #ifndef FFMA_WM
 #define FFMA_WM 4
 #endif
@@ -93,11 +96,26 @@ __device__ __forceinline__ void compute_stage(float (&acc)[C::TM][C::TN], const 
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
             const float av = comp(a[i / 4], i % 4);
+#if FFMA_PACKED
+            // two FP32 lanes per instruction (each lane one fused multiply-add,
+            // rounded once, exactly as fmaf): half the issue slots of scalar FFMA
+            const float2 a2 = make_float2(av, av);
+#pragma unroll
+            for (int qq = 0; qq < TN / 2; ++qq) {
+                const int q = (i & 1) ? TN / 2 - 1 - qq : qq;
+                const float4 &bh = b[q / 2];
+                const float2 b2 = (q & 1) ? make_float2(bh.z, bh.w) : make_float2(bh.x, bh.y);
+                const float2 d = __ffma2_rn(a2, b2, make_float2(acc[i][2 * q], acc[i][2 * q + 1]));
+                acc[i][2 * q] = d.x;
+                acc[i][2 * q + 1] = d.y;
+            }
+#else
 #pragma unroll
             for (int jj = 0; jj < TN; ++jj) {
                 const int j = (i & 1) ? TN - 1 - jj : jj;
                 acc[i][j] = fmaf(av, comp(b[j / 4], j % 4), acc[i][j]);
             }
+#endif
         }
     }
 }

@@ -58,9 +58,9 @@ def test_multi_tile_ragged(M, N, K):
         assert chosen == k
 
 
-DEC_M = [1, 2, 3, 4, 5, 8, 9, 16]
+DEC_M = [1, 2, 3, 4, 5, 8, 9, 12, 16]
 DEC_N = [1, 3, 129, 1000]
-DEC_K = [1, 65, 700, 4097]
+DEC_K = [1, 65, 700, 1028, 4097]
 
 
 @pytest.mark.parametrize("M,N,K", list(itertools.product(DEC_M, DEC_N, DEC_K)))
