@@ -215,10 +215,10 @@ int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t ld
         case SGEMM_KERNEL_DECODE: e = launch_decode(g); break;
         case SGEMM_KERNEL_FFMA_TMA: {
             float *ws = nullptr;
-            const int rc = workspace((size_t)K * (size_t)ffma_tma_at_ld(M) * sizeof(float),
-                                     g.stream, &ws);
+            const int64_t nf = ffma_tma_workspace_floats(g, INT64_MAX);
+            const int rc = workspace((size_t)nf * sizeof(float), g.stream, &ws);
             if (rc != SGEMM_OK) return rc;
-            e = launch_ffma_tma(g, ws);
+            e = launch_ffma_tma(g, ws, nf);
             break;
         }
         case SGEMM_KERNEL_TF32X3: {

@@ -44,13 +44,19 @@ cudaError_t launch_scale_c(const GemmArgs &g);
 cudaError_t launch_ffma_generic(const GemmArgs &g);
 // FFMA kernel: transposes A into `workspace` (K rows of ffma_tma_at_ld(M)
 // floats, 16-byte aligned), then runs the TMA-staged kernel on A^T and B.
-cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace);
+// `capacity` is the workspace's size in floats: at least K * ffma_tma_at_ld(M);
+// whatever ffma_tma_workspace_floats(g, capacity) asks beyond that holds the
+// partial tiles of the split last wave.
+cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace, int64_t capacity);
+int64_t ffma_tma_workspace_floats(const GemmArgs &g, int64_t capacity);
 int64_t ffma_tma_at_ld(int64_t M);
 // Largest M the TMA FFMA kernel's grid can cover.
 int64_t ffma_tma_max_m();
-// At[k*ldt + m] = A[m*lda + k] for m < M, k < K (ldt % 4 == 0, At 16-byte aligned).
+// At[k*ldt + m] = A[m*lda + k] for m < M, k < K (ldt % 4 == 0, At 16-byte aligned);
+// also sets zero[0 .. nzero) to 0 (nzero <= 1024).
 cudaError_t launch_transpose(int64_t M, int64_t K, const float *A, int64_t lda, float *At,
-                             int64_t ldt, cudaStream_t stream);
+                             int64_t ldt, cudaStream_t stream, unsigned *zero = nullptr,
+                             int nzero = 0);
 // TF32 hi/lo split of B (K x N) written transposed: hi[n*ldo + k], lo[n*ldo + k].
 cudaError_t launch_transpose_split(int64_t K, int64_t N, const float *B, int64_t ldb, float *hi,
                                    float *lo, int64_t ldo, cudaStream_t stream);

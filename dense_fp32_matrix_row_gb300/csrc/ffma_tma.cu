@@ -31,8 +31,14 @@
 //
 // Lane (ty, tx) of warp (wm, wn) owns rows    wm*4*TM + 16*(i/4) + 4*ty + i%4   (i < TM)
 //                                 and columns wn*8*TN + 32*(j/4) + 4*tx + j%4   (j < TN).
+#include <algorithm>
+#include <atomic>
+
 #include "common.cuh"
 
+#ifndef FFMA_TAIL_SPLIT
+#define FFMA_TAIL_SPLIT 1
+#endif
 #ifndef FFMA_PACKED
 #define FFMA_PACKED 1
 #endif
@@ -162,39 +168,67 @@ __device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int
     }
 }
 
+// Work units.  Units 0 .. full-1 are whole tiles, tile t = unit t, in
+// row-major tile order (tiles_x tiles along N).  When the last wave of tiles
+// would leave most CTA slots idle, each of the remaining tiles is split into
+// `parts` ranges of kt_part k-tiles: unit full + r*parts + p computes part p
+// of tile full + r, writes its partial tile to `partials`, and the unit that
+// finishes a tile last (counted in counters[r], zeroed before the launch)
+// sums the parts in part order and applies the epilogue -- no unit waits for
+// another.
+struct TailSplit {
+    int tiles_x;
+    int full;
+    int parts;
+    int kt_part;
+    float *partials;      // [(tiles - full) * parts][THREADS * TM * TN]
+    unsigned *counters;   // [tiles - full]
+};
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmB,
                 int M, int N, int K, float alpha, float beta, float *__restrict__ Cm, int64_t ldc,
-                int c_vec4, unsigned *err, uint64_t wait_ns) {
+                int c_vec4, TailSplit ts, unsigned *err, uint64_t wait_ns) {
     constexpr int TM = C::TM, TN = C::TN, BK = C::BK, BM = C::BM, BN = C::BN, STAGES = C::STAGES;
     extern __shared__ unsigned char smem_raw[];
+    __shared__ unsigned s_prev;
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127);
     float *sA = reinterpret_cast<float *>(base);
     float *sB = sA + STAGES * C::A_STAGE;
     uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * C::B_STAGE);
     unsigned *arrived = reinterpret_cast<unsigned *>(full + STAGES);   // warps done with a stage
-    int *issued = reinterpret_cast<int *>(arrived + STAGES);           // k-tile last copied in
+    int *issued = reinterpret_cast<int *>(arrived + STAGES);           // local k-tile last copied in
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
     const int ktiles = (K + BK - 1) / BK;
+    const int unit = blockIdx.x;
+    int tile = unit, part = -1, kt0 = 0, kt1 = ktiles;
+    if (unit >= ts.full) {
+        const int v = unit - ts.full;
+        tile = ts.full + v / ts.parts;
+        part = v % ts.parts;
+        kt0 = part * ts.kt_part;
+        kt1 = min(kt0 + ts.kt_part, ktiles);
+    }
+    const int m0 = (tile / ts.tiles_x) * BM, n0 = (tile % ts.tiles_x) * BN;
+    const int nkt = kt1 > kt0 ? kt1 - kt0 : 0;
 
-    // Copy k-tile kt into stage kt % STAGES (one thread).
-    auto issue = [&](int kt) {
-        const int s = kt % STAGES;
-        issued[s] = kt;
+    // Copy local k-tile j (k-tile kt0 + j) into stage j % STAGES (one thread).
+    auto issue = [&](int j) {
+        const int s = j % STAGES;
+        issued[s] = j;
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-        tma_load_2d(smem_u32(sA + s * C::A_STAGE), &tmAt, fb, m0, kt * BK);
-        tma_load_2d(smem_u32(sB + s * C::B_STAGE), &tmB, fb, n0, kt * BK);
+        tma_load_2d(smem_u32(sA + s * C::A_STAGE), &tmAt, fb, m0, (kt0 + j) * BK);
+        tma_load_2d(smem_u32(sB + s * C::B_STAGE), &tmB, fb, n0, (kt0 + j) * BK);
     };
     // After a failed wait: wait for every copy issued so far, so that none
     // lands in this block's shared memory after the block has exited.
     auto drain = [&]() {
         for (int s = 0; s < STAGES; ++s) {
-            const int kt = *reinterpret_cast<volatile int *>(&issued[s]);
-            if (kt >= 0) mbar_wait(smem_u32(&full[s]), (kt / STAGES) & 1, DRAIN_NS);
+            const int j = *reinterpret_cast<volatile int *>(&issued[s]);
+            if (j >= 0) mbar_wait(smem_u32(&full[s]), (j / STAGES) & 1, DRAIN_NS);
         }
     };
 
@@ -211,7 +245,7 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmAt);
         tma_prefetch_desc(&tmB);
-        for (int kt = 0; kt < STAGES && kt < ktiles; ++kt) issue(kt);
+        for (int j = 0; j < STAGES && j < nkt; ++j) issue(j);
     }
 
     const int wm = warp / C::WN, wn = warp % C::WN;
@@ -225,14 +259,13 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
-    for (int kt = 0; kt < ktiles; ++kt) {
-        const int s = kt % STAGES;
-        if (!mbar_wait(smem_u32(&full[s]), (kt / STAGES) & 1, wait_ns)) {
-            if (lane == 0) {
-                record_error(err, kErrWaitTimeout);
-                drain();
-            }
-            return;
+    bool failed = false;
+    for (int j = 0; j < nkt; ++j) {
+        const int s = j % STAGES;
+        if (!mbar_wait(smem_u32(&full[s]), (j / STAGES) & 1, wait_ns)) {
+            failed = true;
+            if (lane == 0) record_error(err, kErrWaitTimeout);
+            break;
         }
         compute_stage<C>(acc, sA + s * C::A_STAGE + arow, sB + s * C::B_STAGE + bcol);
         // Release the stage; the last warp to do so refills it STAGES k-tiles ahead.
@@ -241,20 +274,123 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
             __threadfence_block();
             if (atomicAdd(&arrived[s], 1u) == C::WARPS - 1) {
                 arrived[s] = 0;
-                if (kt + STAGES < ktiles) {
+                if (j + STAGES < nkt) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue(kt + STAGES);
+                    issue(j + STAGES);
                 }
             }
         }
     }
+    // Every warp is past the loop, so `issued` no longer changes.
+    const bool any_failed = __syncthreads_or(failed) != 0;
+    if (any_failed && threadIdx.x == 0) drain();
 
     // ---------------------------------------------------------------- epilogue
+    if (part < 0) {
+        if (!any_failed) store_tile<C>(acc, m0, n0, arow, bcol, M, N, alpha, beta, Cm, ldc, c_vec4);
+        return;
+    }
+    // Partial tile, thread-interleaved so that each warp writes whole lines.
+    constexpr int NV = TM * TN / 4;
+    float4 *mine = reinterpret_cast<float4 *>(ts.partials) + (size_t)(unit - ts.full) * NV * C::THREADS;
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int h = 0; h < TN / 4; ++h)
+            __stcg(mine + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x,
+                   make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]));
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_prev = atomicAdd(&ts.counters[tile - ts.full], 1u);
+    __syncthreads();
+    if (s_prev != (unsigned)(ts.parts - 1)) return;
+    __threadfence();
+    // Last part in: sum parts 0 .. parts-1 in that order (own part included),
+    // independent of which unit arrived last.
+    const float4 *first = reinterpret_cast<const float4 *>(ts.partials) +
+                          (size_t)(tile - ts.full) * ts.parts * NV * C::THREADS;
+    for (int q = 0; q < ts.parts; ++q) {
+        const float4 *src = first + (size_t)q * NV * C::THREADS;
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int h = 0; h < TN / 4; ++h) {
+                const float4 v = __ldcg(src + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x);
+                if (q == 0) {
+                    acc[i][4 * h] = v.x; acc[i][4 * h + 1] = v.y;
+                    acc[i][4 * h + 2] = v.z; acc[i][4 * h + 3] = v.w;
+                } else {
+                    acc[i][4 * h] += v.x; acc[i][4 * h + 1] += v.y;
+                    acc[i][4 * h + 2] += v.z; acc[i][4 * h + 3] += v.w;
+                }
+            }
+    }
     store_tile<C>(acc, m0, n0, arow, bcol, M, N, alpha, beta, Cm, ldc, c_vec4);
 }
 
+// CTAs of the kernel one SM holds, per device (0 until asked).
 template <class C>
-cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt) {
+int ctas_per_sm() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaFuncSetAttribute(ffma_tma_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::SMEM) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ffma_tma_kernel<C>, C::THREADS, C::SMEM) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// The work list for one call.  The tail split is used when the tiles left
+// over after the last full wave of CTA slots fill at most half a wave, each
+// part keeps at least four k-tiles, and the partial tiles fit in `capacity`
+// floats of workspace beside A^T.
+struct Plan {
+    int tiles_x = 0;
+    int64_t tiles = 0, full = 0;
+    int parts = 1, kt_part = 0;
+    int64_t tail() const { return tiles - full; }
+    int64_t units() const { return full + tail() * parts; }
+};
+constexpr int64_t kCounterFloats = 1024;   // counters reserved after A^T
+constexpr int64_t kMaxParts = 16;
+
+template <class C>
+int64_t partial_floats(const Plan &p) {
+    return p.parts > 1 ? kCounterFloats + p.tail() * p.parts * (int64_t)C::BM * C::BN : 0;
+}
+
+template <class C>
+Plan plan_units(const GemmArgs &g, int64_t at_floats, int64_t capacity) {
+    Plan p;
+    p.tiles_x = (int)((g.N + C::BN - 1) / C::BN);
+    p.tiles = (int64_t)p.tiles_x * ((g.M + C::BM - 1) / C::BM);
+    p.full = p.tiles;
+    const int64_t slots = (int64_t)ctas_per_sm<C>() * g.sm_count;
+    const int64_t ktiles = (g.K + C::BK - 1) / C::BK;
+    if (slots <= 0 || !FFMA_TAIL_SPLIT) return p;
+    const int64_t rem = p.tiles % slots;
+    if (rem == 0 || 2 * rem > slots || rem > kCounterFloats) return p;
+    int parts = (int)std::min<int64_t>(std::min<int64_t>(slots / rem, kMaxParts), ktiles / 4);
+    Plan q = p;
+    q.full = p.tiles - rem;
+    for (; parts >= 2; --parts) {
+        q.parts = parts;
+        if (at_floats + partial_floats<C>(q) <= capacity) break;
+    }
+    if (parts < 2) return p;
+    q.kt_part = (int)((ktiles + parts - 1) / parts);
+    return q;
+}
+
+template <class C>
+cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt, const Plan &p, float *extra) {
     alignas(64) CUtensorMap tmAt, tmB;
     if (!encode_tma_2d(g.encode, &tmAt, At, g.M, g.K, ldt, C::BM, C::BK, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, C::BN, C::BK, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -263,11 +399,17 @@ cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt) {
     cudaError_t e = cudaFuncSetAttribute(ffma_tma_kernel<C>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((g.N + C::BN - 1) / C::BN), (unsigned)((g.M + C::BM - 1) / C::BM));
-    if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+    if (p.units() > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    TailSplit ts;
+    ts.tiles_x = p.tiles_x;
+    ts.full = (int)p.full;
+    ts.parts = p.parts;
+    ts.kt_part = p.kt_part;
+    ts.counters = reinterpret_cast<unsigned *>(extra);
+    ts.partials = extra != nullptr ? extra + kCounterFloats : nullptr;
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
-    ffma_tma_kernel<C><<<grid, C::THREADS, C::SMEM, g.stream>>>(
-        tmAt, tmB, (int)g.M, (int)g.N, (int)g.K, g.alpha, g.beta, g.C, g.ldc, c_vec4, g.err,
+    ffma_tma_kernel<C><<<(unsigned)p.units(), C::THREADS, C::SMEM, g.stream>>>(
+        tmAt, tmB, (int)g.M, (int)g.N, (int)g.K, g.alpha, g.beta, g.C, g.ldc, c_vec4, ts, g.err,
         g.wait_ns);
     return cudaGetLastError();
 }
@@ -278,11 +420,20 @@ int64_t ffma_tma_max_m() { return (int64_t)65535 * Default::BM; }
 
 int64_t ffma_tma_at_ld(int64_t M) { return (M + 3) / 4 * 4; }
 
-cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace) {
+int64_t ffma_tma_workspace_floats(const GemmArgs &g, int64_t capacity) {
+    const int64_t at = g.K * ffma_tma_at_ld(g.M);
+    return at + partial_floats<Default>(plan_units<Default>(g, at, capacity));
+}
+
+cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace, int64_t capacity) {
     const int64_t ldt = ffma_tma_at_ld(g.M);
-    cudaError_t e = launch_transpose(g.M, g.K, g.A, g.lda, workspace, ldt, g.stream);
+    const int64_t at = g.K * ldt;
+    const Plan p = plan_units<Default>(g, at, capacity);
+    float *extra = p.parts > 1 ? workspace + at : nullptr;
+    cudaError_t e = launch_transpose(g.M, g.K, g.A, g.lda, workspace, ldt, g.stream,
+                                     reinterpret_cast<unsigned *>(extra), (int)(p.parts > 1 ? p.tail() : 0));
     if (e != cudaSuccess) return e;
-    return launch_cfg<Default>(g, workspace, ldt);
+    return launch_cfg<Default>(g, workspace, ldt, p, extra);
 }
 
 }  // namespace sgemm_gb300

@@ -63,5 +63,5 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const
     g.stream = static_cast<cudaStream_t>(stream);
     rc = fill_device_args(g);
     if (rc != SGEMM_OK) return rc;
-    return launch_ffma_tma(g, scratch) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+    return launch_ffma_tma(g, scratch, kScratchFloats) == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
 }

@@ -36,8 +36,10 @@ template <bool SPLIT>
 __global__ void __launch_bounds__(TTHREADS)
 transpose_tile_kernel(int64_t R, int64_t Cc, const float *__restrict__ src, int64_t lds,
                       int src_vec, float *__restrict__ dst_hi, float *__restrict__ dst_lo,
-                      int64_t ldd) {
+                      int64_t ldd, unsigned *__restrict__ zero, int nzero) {
     __shared__ float tile[TD][TD + 1];
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < nzero; i += TTHREADS) zero[i] = 0u;
     const int64_t r0 = (int64_t)blockIdx.y * TD, c0 = (int64_t)blockIdx.x * TD;
     const int t = threadIdx.x;
     const int q = t & 15;         // float4 column within the tile
@@ -145,20 +147,24 @@ inline int vec_ok(const float *p, int64_t ld) {
 
 template <bool SPLIT>
 cudaError_t launch_tile(int64_t R, int64_t Cc, const float *src, int64_t lds, float *hi, float *lo,
-                        int64_t ldd, cudaStream_t stream) {
+                        int64_t ldd, cudaStream_t stream, unsigned *zero = nullptr, int nzero = 0) {
     const int64_t gx = (Cc + TD - 1) / TD, gy = (R + TD - 1) / TD;
-    if (gy > 65535 || gx > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    if (gx == 0 || gy == 0) return cudaSuccess;
+    if (gy > 65535 || gx > 0x7fffffff || nzero < 0 || nzero > 1024 || (nzero > 0 && zero == nullptr))
+        return cudaErrorInvalidConfiguration;
+    if (gx == 0 || gy == 0) {
+        if (nzero > 0) return cudaMemsetAsync(zero, 0, (size_t)nzero * sizeof(unsigned), stream);
+        return cudaSuccess;
+    }
     transpose_tile_kernel<SPLIT><<<dim3((unsigned)gx, (unsigned)gy), TTHREADS, 0, stream>>>(
-        R, Cc, src, lds, vec_ok(src, lds), hi, lo, ldd);
+        R, Cc, src, lds, vec_ok(src, lds), hi, lo, ldd, zero, nzero);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_transpose(int64_t M, int64_t K, const float *A, int64_t lda, float *At,
-                             int64_t ldt, cudaStream_t stream) {
-    return launch_tile<false>(M, K, A, lda, At, nullptr, ldt, stream);
+                             int64_t ldt, cudaStream_t stream, unsigned *zero, int nzero) {
+    return launch_tile<false>(M, K, A, lda, At, nullptr, ldt, stream, zero, nzero);
 }
 
 cudaError_t launch_transpose_split(int64_t K, int64_t N, const float *B, int64_t ldb, float *hi,

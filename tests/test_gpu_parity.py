@@ -342,6 +342,26 @@ def test_large_ragged_full_compare(M, N, K, beta):
     assert chosen == TMA
 
 
+# Shapes whose last wave is split along K (tiles over 304 resident blocks on
+# a 152-SM GB300: 1000^3 has 64 tiles in 4 parts each, 1500x1100x700 has 108
+# tiles in 2 parts); every output compared, and a second call is bitwise equal.
+@pytest.mark.parametrize("M,N,K,beta,ldc_pad", [(1000, 1000, 1000, 0.0, 0), (1500, 1100, 700, -0.4, 5),
+                                                (1001, 999, 513, 1.0, 3)])
+def test_split_last_wave(M, N, K, beta, ldc_pad):
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=M + N + K, beta=beta)
+    ldb = (N + 3) // 4 * 4
+    _, chosen = run_checked(sg, A, B, C0, 0.8, beta, lds=(K, ldb, N + ldc_pad))
+    assert chosen == TMA
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    outs = []
+    for _ in range(2):
+        dC = torch.from_numpy(C0).cuda()
+        sg.sgemm(dA, dB, dC, 0.8, beta)
+        assert sg.status() == sg.OK
+        outs.append(dC.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])
+
+
 def test_large_small_integers_exact():
     A, B, C0 = make_inputs(2200, 2400, 300, "int", seed=9, beta=-1.0)
     _, chosen = run_checked(sg, A, B, C0, 2.0, -1.0, exact=True)
