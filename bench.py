@@ -253,12 +253,17 @@ def timed_steps(fn, steps, stream):
 
 def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3):
     """Device-timed secondary shapes on device-generated data (timing only;
-    parity for these shapes is covered by the test suite)."""
+    parity for these shapes is covered by the test suite).  "ms" is per call
+    in a replayed CUDA graph; "ms_eager" per call with an event pair around
+    each eager call."""
     out = {}
     g = torch.Generator(device=dev)
     g.manual_seed(3)
 
     def bench_shape(M, N, K, sigma_b, tensor_cores=False):
+        """Mean ms per call of `steps` calls captured in one CUDA graph and
+        replayed (the launch gaps of eager calls excluded), after warm-up calls
+        that also size the workspace so that capture allocates nothing."""
         A = torch.randn((M, K), device=dev, generator=g)
         B = torch.randn((K, N), device=dev, generator=g) * sigma_b
         C = torch.empty((M, N), device=dev)
@@ -266,31 +271,53 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3):
         for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
-        _, per = timed_steps(fn, steps, stream)
+        _, per_eager = timed_steps(fn, steps, stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(steps):
+                fn()
+        with torch.cuda.stream(stream):
+            graph.replay()                      # warm replay
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        per = e0.elapsed_time(e1) / steps
         st = sg.status(stream)
         kid = sg.select_kernel(M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), N, 0.0,
                                C.data_ptr(), N, tensor_cores)
-        del A, B, C
-        return per, st, sg.KERNEL_NAMES.get(kid, str(kid))
+        del A, B, C, graph
+        return per, st, sg.KERNEL_NAMES.get(kid, str(kid)), per_eager
 
     for M in (1, 4, 16):
         N, K = 14336, 4096
-        per, st, kn = bench_shape(M, N, K, 0.02)
+        per, st, kn, pe = bench_shape(M, N, K, 0.02)
         nbytes = 4 * (M * K + K * N + M * N)
         gbs = nbytes / (per * 1e-3) / 1e9
         out[f"decode_m{M}"] = {"shape": [M, N, K], "kernel": kn, "ms": per, "GB/s": gbs,
                                "frac_hbm": gbs / peaks["hbm_gbs"], "status": st,
-                               "TFLOP/s": 2 * M * N * K / (per * 1e-3) / 1e12}
+                               "TFLOP/s": 2 * M * N * K / (per * 1e-3) / 1e12,
+                               "ms_eager": pe, "GB/s_eager": nbytes / (pe * 1e-3) / 1e9}
     big = [("sgemm_8192", 8192, 8192, 8192, 1.0), ("prefill_qkv", 8192, 12288, 4096, 0.02),
            ("prefill_up", 8192, 14336, 4096, 0.02), ("prefill_down", 8192, 4096, 14336, 0.02)]
     for name, M, N, K, sb in big:
-        per, st, kn = bench_shape(M, N, K, sb)
+        per, st, kn, pe = bench_shape(M, N, K, sb)
         out[name] = {"shape": [M, N, K], "kernel": kn, "ms": per, "status": st,
-                     "TFLOP/s": 2 * M * N * K / (per * 1e-3) / 1e12}
-    per, st, kn = bench_shape(8192, 8192, 8192, 1.0, tensor_cores=True)
+                     "TFLOP/s": 2 * M * N * K / (per * 1e-3) / 1e12, "ms_eager": pe}
+    # Medium and skinny shapes whose last wave is split along K.  Their
+    # operands (4-34 MB) stay in L2 between repetitions: timing only.
+    mid = [("mid_1024", 1024, 1024, 1024), ("mid_1024x1024x8192", 1024, 1024, 8192),
+           ("mid_512x512x8192", 512, 512, 8192), ("mid_2048", 2048, 2048, 2048)]
+    for name, M, N, K in mid:
+        per, st, kn, pe = bench_shape(M, N, K, 1.0)
+        out[name] = {"shape": [M, N, K], "kernel": kn, "ms": per, "status": st, "l2_resident": True,
+                     "TFLOP/s": 2 * M * N * K / (per * 1e-3) / 1e12, "ms_eager": pe}
+    per, st, kn, pe = bench_shape(8192, 8192, 8192, 1.0, tensor_cores=True)
     useful = 2 * 8192**3 / (per * 1e-3) / 1e12
     tf32_peak = peaks["bf16_tflops"] * 1.1 / 2.25   # measured bf16 x nominal tf32/bf16
-    out["sgemm_8192_3xtf32"] = {"shape": [8192, 8192, 8192], "kernel": kn, "ms": per,
+    out["sgemm_8192_3xtf32"] = {"shape": [8192, 8192, 8192], "kernel": kn, "ms": per, "ms_eager": pe,
                                 "status": st, "TFLOP/s": useful,
                                 "tensor_TFLOP/s": 3 * useful, "tf32_peak": tf32_peak,
                                 "frac_tf32_peak": 3 * useful / tf32_peak,

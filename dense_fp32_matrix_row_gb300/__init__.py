@@ -21,6 +21,7 @@ __all__ = ["sgemm", "sgemm_3xtf32", "sgemm_ptr", "status", "select_kernel", "for
 OK = 0
 ERR_BAD_DIM, ERR_BAD_LD, ERR_NULL_PTR, ERR_ALIAS = -1, -2, -3, -4
 ERR_CUDA, ERR_DEVICE, ERR_TIMEOUT, ERR_BAD_ARG = -5, -6, -7, -8
+ERR_TOO_LARGE, ERR_CAPTURE = -9, -10
 
 KERNEL_AUTO, KERNEL_NONE, KERNEL_SCALE_C, KERNEL_FFMA_TMA = 0, 1, 2, 3
 KERNEL_FFMA_GENERIC, KERNEL_DECODE, KERNEL_TF32X3 = 4, 5, 6

@@ -49,6 +49,13 @@ int workspace(size_t bytes, cudaStream_t s, float **out) {
     std::lock_guard<std::mutex> lock(g_ws_mu);
     auto &w = g_ws[{dev, reinterpret_cast<uintptr_t>(s)}];
     if (w.second < bytes) {
+        // An allocation made while `s` is captured would belong to the graph.
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return SGEMM_ERR_CUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return SGEMM_ERR_CAPTURE;
         const size_t grow = std::max(bytes, w.second + w.second / 2);
         const size_t nb = (grow + (size_t(2) << 20) - 1) & ~((size_t(2) << 20) - 1);
         if (w.first != nullptr) {
@@ -323,6 +330,9 @@ const char *sgemm_status_string(int status) {
         case SGEMM_ERR_DEVICE: return "the current device is not an sm_103 GPU";
         case SGEMM_ERR_TIMEOUT: return "a device-side bounded wait ran out";
         case SGEMM_ERR_BAD_ARG: return "invalid argument";
+        case SGEMM_ERR_CAPTURE:
+            return "the stream is being captured and the call needs a larger workspace; "
+                   "run one call of this shape eagerly on the stream first";
         case SGEMM_ERR_TOO_LARGE:
             return "problem needs more than the fixed scratch of sgemm_noalloc "
                    "(K * round_up(M, 4) floats > 16777216)";

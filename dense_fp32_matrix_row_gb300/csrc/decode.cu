@@ -28,6 +28,10 @@
 
 namespace cg = cooperative_groups;
 
+#ifndef DECODE_PACKED
+#define DECODE_PACKED 0
+#endif
+
 namespace sgemm_gb300 {
 namespace {
 
@@ -389,10 +393,20 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int
     cluster.sync();
 }
 
-// acc[j] += a * b[j] for j < 8, as packed two-lane FP32 FMAs (each lane a
-// fused multiply-add rounded once, exactly as fmaf); `rev` walks the pairs
-// backwards (alternating rows keep operands of neighbouring FMAs apart).
+// acc[j] += a * b[j] for j < 8; `rev` walks the columns backwards
+// (alternating rows keep operands of neighbouring FMAs apart).  Scalar FFMA
+// by default: the packed two-lane form needs `a` duplicated into a register
+// pair, and those moves cost more than the packed issue saves here, where the
+// FMA pipe, not issue, is the limit (measured at M = 16: 4.40 vs 4.53 TB/s).
 __device__ __forceinline__ void fma_row8(float (&acc)[8], float a, const float (&b)[8], bool rev) {
+#if !DECODE_PACKED
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+        const int j = rev ? 7 - jj : jj;
+        acc[j] = fmaf(a, b[j], acc[j]);
+    }
+    return;
+#endif
     const float2 a2 = make_float2(a, a);
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq) {
@@ -621,13 +635,19 @@ constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32, DO_TKB = 
 #define DECODE_DO_STAGES 2
 #endif
 #ifndef DECODE_DO_MINB
-#define DECODE_DO_MINB 4
+#define DECODE_DO_MINB 0   // blocks per SM the registers are sized for; 0: by row count
+#endif
+#ifndef DECODE_DO_KS
+#define DECODE_DO_KS 0
 #endif
 constexpr int DO_STAGES = DECODE_DO_STAGES;
 constexpr int DO_KSMAX = 16;   // cluster size limit (16 is non-portable)
 
 template <int MT, int RG>
 struct DoCfg {
+    // 64 accumulators per lane at MT/RG = 8: five blocks per SM (96 registers)
+    // suit M <= 8; at M = 16, four blocks (128 registers) measured faster.
+    static constexpr int MINB = DECODE_DO_MINB > 0 ? DECODE_DO_MINB : (MT <= 8 ? 5 : 4);
     static constexpr int KG = DO_WARPS / RG;                               // k groups
     static constexpr int MTL = MT / RG;                                    // rows per lane
     static constexpr int RPW = DO_TKB / KG;                                // k-steps per warp per stage
@@ -644,7 +664,7 @@ struct DoCfg {
 };
 
 template <int MT, int RG>
-__global__ void __launch_bounds__(DO_THREADS, DECODE_DO_MINB)
+__global__ void __launch_bounds__(DO_THREADS, DoCfg<MT, RG>::MINB)
 decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
                     int M, int64_t N, int64_t K, float alpha, float beta, float *__restrict__ C,
                     int64_t ldc, int64_t kslice, unsigned *err, uint64_t wait_ns) {
@@ -949,7 +969,8 @@ cudaError_t launch_outer(const GemmArgs &g) {
     cfg.blockDim = dim3(DO_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::BYTES;
     cfg.stream = g.stream;
-    const int ks = choose_cluster(kern, g.K, ncb, ksmax, DO_TKB, cfg, cache);
+    int ks = choose_cluster(kern, g.K, ncb, ksmax, DO_TKB, cfg, cache);
+    if (DECODE_DO_KS > 0 && g.K / DECODE_DO_KS >= DO_TKB) ks = DECODE_DO_KS;
     int64_t kslice = (g.K + ks - 1) / ks;
     kslice = (kslice + DO_TKB - 1) / DO_TKB * DO_TKB;
 

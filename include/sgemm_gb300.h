@@ -68,6 +68,7 @@ extern "C" {
 #define SGEMM_ERR_TIMEOUT    -7   /* a device-side bounded wait ran out (from sgemm_status) */
 #define SGEMM_ERR_BAD_ARG    -8   /* any other invalid argument */
 #define SGEMM_ERR_TOO_LARGE  -9   /* beyond sgemm_noalloc's fixed scratch */
+#define SGEMM_ERR_CAPTURE   -10   /* the stream is being captured and the call would allocate */
 
 /* Kernel identifiers, for sgemm_select_kernel and sgemm_force_kernel. */
 #define SGEMM_KERNEL_AUTO          0   /* library's choice (sgemm_force_kernel only) */
@@ -98,6 +99,11 @@ extern "C" {
  * split-K reduction of "CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section
  * "10", applied to the last wave only).  The result is deterministic: the
  * same inputs give the same bits on every call on the same GPU model.
+ * CUDA graphs: calls can be captured on `stream` (and the graph replayed)
+ * once a call of the same shape has run eagerly on the same stream and
+ * device: that call sets up the device and sizes the stream's workspace.  A
+ * captured call never allocates: one that would need a larger workspace
+ * returns SGEMM_ERR_CAPTURE with nothing enqueued.
  * Returns SGEMM_OK, or an argument/launch error code (nothing enqueued).
  */
 int sgemm(int64_t M, int64_t N, int64_t K, float alpha,

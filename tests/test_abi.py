@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings(L):
-    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10):
         s = sg.status_string(code)
         assert s and s != "unknown status"
     assert sg.status_string(12345) == "unknown status"
