@@ -418,218 +418,26 @@ __device__ __forceinline__ void fma_row8(float (&acc)[8], float a, const float (
     }
 }
 
-// ---------------------------------------------------------------- tile variant (M >= 5)
-// The FFMA tile kernel's layout applied to the skinny product: a block owns
-// an MT x 256 tile of C; lane (ty, tx) of warp w owns rows ty*(MT/4) ..
-// +MT/4-1 and the eight columns w*64 + tx*4 + {0..3} and +32, an (MT/4) x 8
-// register outer product per k.  Every output belongs to one thread, so
-// there is no reduction across warps, and at 80 registers six blocks share
-// an SM.
-//
-// Each stage of the TMA ring carries both operands of DT_TKB k-steps: the
-// DT_TKB x 256 panel of B and the MT x DT_TKB panel of A (row-major, rows
-// past M zero-filled by the copy).  A lane reads its A rows four k at a time
-// with one 128-bit load per row, so the K loop has no block barrier and no
-// global load of its own: every wait is on a copy that was issued
-// DT_STAGES - 1 panels earlier.  Requires A and B 16-byte aligned with
-// lda % 4 == 0 and ldb % 4 == 0.
-//
-// K is split over the blocks of a cluster of up to DT_KSMAX (16 needs the
-// non-portable cluster size); the launcher takes the largest split whose
-// clusters all fit on the GPU at once.
-constexpr int DT_COLS = 256, DT_WARPS = 4, DT_THREADS = DT_WARPS * 32;
-#ifndef DECODE_DT_TKB
-#define DECODE_DT_TKB 16
-#endif
-#ifndef DECODE_DT_STAGES
-#define DECODE_DT_STAGES 2
-#endif
-#ifndef DECODE_DT_MINB
-#define DECODE_DT_MINB 6
-#endif
-#ifndef DECODE_DT_KSMAX
-#define DECODE_DT_KSMAX 16
-#endif
-constexpr int DT_TKB = DECODE_DT_TKB, DT_STAGES = DECODE_DT_STAGES, DT_KSMAX = DECODE_DT_KSMAX;
-
-template <int MT>
-struct DtCfg {
-    static constexpr int TM = MT / 4;                                      // rows per lane
-    static constexpr size_t B_PANEL = (size_t)DT_TKB * DT_COLS;            // floats, [k][n]
-    static constexpr size_t A_PANEL = (size_t)MT * DT_TKB;                 // floats, [m][k]
-    static constexpr size_t STAGE = B_PANEL + A_PANEL;
-    static constexpr size_t RING = DT_STAGES * STAGE;
-    static constexpr size_t PART = (size_t)MT * DT_COLS;                  // aliases the ring
-    static constexpr size_t REGION0 = RING > PART ? RING : PART;
-    static constexpr size_t BYTES = 128 + REGION0 * 4 + DT_STAGES * 16;
-    static_assert(MT % 4 == 0 && MT >= 8, "four row groups of lanes");
-    static_assert(DT_TKB % 4 == 0, "A rows are read four k at a time");
-    static_assert((STAGE * 4) % 128 == 0, "stage offsets stay 128-byte aligned");
-    static_assert(DT_KSMAX == 8 || DT_KSMAX == 16, "cluster size");
-};
-
-template <int MT>
-__global__ void __launch_bounds__(DT_THREADS, DECODE_DT_MINB)
-decode_tile_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
-                   int M, int64_t N, int64_t K, float alpha, float beta, float *__restrict__ C,
-                   int64_t ldc, int64_t kslice, unsigned *err, uint64_t wait_ns) {
-    using L = DtCfg<MT>;
-    constexpr int TM = L::TM;
-    extern __shared__ unsigned char smem_raw[];
-    float *smem = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
-                                            ~uintptr_t(127));
-    float *ring = smem;                    // [DT_STAGES][B panel | A panel]
-    float *part = smem;                    // [MT][DT_COLS], after the K loop
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::REGION0);
-    unsigned *arrived = reinterpret_cast<unsigned *>(full + DT_STAGES);
-    int *issued = reinterpret_cast<int *>(arrived + DT_STAGES);
-
-    cg::cluster_group cluster = cg::this_cluster();
-    const int rank = (int)cluster.block_rank();
-    const int ks = (int)cluster.num_blocks();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ty = lane >> 3, tx = lane & 7;
-    const int64_t n0 = (int64_t)blockIdx.y * DT_COLS;
-    const int64_t kbeg = (int64_t)rank * kslice;
-    const int64_t kend = (kbeg + kslice < K) ? kbeg + kslice : K;
-    const int nst = kend > kbeg ? (int)((kend - kbeg + DT_TKB - 1) / DT_TKB) : 0;
-    const int bcol = warp * 64 + tx * 4;
-
-    auto issue = [&](int st) {
-        const int s = st % DT_STAGES;
-        issued[s] = st;
-        const uint32_t fb = smem_u32(&full[s]);
-        const int32_t kc = (int32_t)(kbeg + (int64_t)st * DT_TKB);
-        float *stg = ring + s * L::STAGE;
-        mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE * 4));
-        tma_load_2d(smem_u32(stg), &tmB, fb, (int32_t)n0, kc);
-        tma_load_2d(smem_u32(stg + L::B_PANEL), &tmA, fb, kc, 0);
-    };
-    auto drain = [&]() {
-        for (int s = 0; s < DT_STAGES; ++s) {
-            const int st = *reinterpret_cast<volatile int *>(&issued[s]);
-            if (st >= 0) mbar_wait(smem_u32(&full[s]), (st / DT_STAGES) & 1, DRAIN_NS);
-        }
-    };
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < DT_STAGES; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            arrived[s] = 0;
-            issued[s] = -1;
-        }
-        mbar_fence_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        tma_prefetch_desc(&tmB);
-        tma_prefetch_desc(&tmA);
-        for (int st = 0; st < DT_STAGES && st < nst; ++st) issue(st);
-    }
-
-    float acc[TM][8];
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-    bool failed = false;
-
-    for (int st = 0; st < nst; ++st) {
-        const int s = st % DT_STAGES;
-        if (!mbar_wait(smem_u32(&full[s]), (st / DT_STAGES) & 1, wait_ns)) {
-            failed = true;
-            if (lane == 0) {
-                record_error(err, kErrWaitTimeout);
-                drain();
-            }
-            break;
-        }
-        const float *stg = ring + s * L::STAGE;
-        const float *bst = stg + bcol;
-        const float *ast = stg + L::B_PANEL + (size_t)ty * TM * DT_TKB;
-#pragma unroll
-        for (int r4 = 0; r4 < DT_TKB; r4 += 4) {
-            float4 av[TM];
-#pragma unroll
-            for (int i = 0; i < TM; ++i)
-                av[i] = *reinterpret_cast<const float4 *>(ast + i * DT_TKB + r4);
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const int r = r4 + rr;
-                const float4 b0 = *reinterpret_cast<const float4 *>(bst + r * DT_COLS);
-                const float4 b1 = *reinterpret_cast<const float4 *>(bst + r * DT_COLS + 32);
-                const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-                for (int i = 0; i < TM; ++i) {
-                    const float a = rr == 0 ? av[i].x : rr == 1 ? av[i].y : rr == 2 ? av[i].z : av[i].w;
-                    fma_row8(acc[i], a, bv, i & 1);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0) {
-            __threadfence_block();
-            if (atomicAdd(&arrived[s], 1u) == DT_WARPS - 1) {
-                arrived[s] = 0;
-                if (st + DT_STAGES < nst) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue(st + DT_STAGES);
-                }
-            }
-        }
-    }
-
-    // After a time-out the warp that saw it waited for every copy in flight;
-    // the others may have stopped at an earlier stage, so wait for all here.
-    if (threadIdx.x == 0) drain();
-    const bool any_failed = __syncthreads_or(failed) != 0;
-    // Each thread's partial tile to shared memory (the ring is free now).
-#pragma unroll
-    for (int i = 0; i < TM; ++i) {
-        float *pr = part + (size_t)(ty * TM + i) * DT_COLS + bcol;
-        *reinterpret_cast<float4 *>(pr) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-        *reinterpret_cast<float4 *>(pr + 32) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
-    }
-    cluster.sync();
-    const int total = MT * DT_COLS;
-    const int per = (total + ks - 1) / ks;
-    const int obeg = rank * per;
-    const int oend = (obeg + per < total) ? obeg + per : total;
-    for (int o = obeg + threadIdx.x; o < oend; o += DT_THREADS) {
-        // independent remote loads first, then the sum in rank order
-        float pv[DT_KSMAX];
-#pragma unroll
-        for (int q = 0; q < DT_KSMAX; ++q) pv[q] = q < ks ? cluster.map_shared_rank(part, q)[o] : 0.0f;
-        float sum = pv[0];
-#pragma unroll
-        for (int q = 1; q < DT_KSMAX; ++q)
-            if (q < ks) sum += pv[q];
-        const int m = o / DT_COLS;
-        const int64_t gn = n0 + (o - m * DT_COLS);
-        if (!any_failed && m < M && gn < N) {
-            float *p = C + (int64_t)m * ldc + gn;
-            const float v = alpha * sum;
-            *p = (beta != 0.0f) ? fmaf(beta, *p, v) : v;
-        }
-    }
-    cluster.sync();
-}
-
 // ---------------------------------------------------------------- outer-product variant (M >= 5)
-// The four warps of a block split the block's MT x 256 tile into RG row
-// groups and every stage's k-steps into KG = 4/RG interleaved k groups.  A
-// lane owns the MT/RG rows of its row group and eight columns (lane*4 +
-// {0..3} and 128 + lane*4 + {0..3}): an (MT/RG) x 8 outer product per k.
-// Per k a lane loads 8 floats of B (two 128-bit loads) and MT/RG broadcast
-// floats of A, so shared memory delivers (MT/RG + 8) floats per lane for
-// 8*MT/RG FFMAs: 0.25 wavefronts per FFMA at MT/RG = 8, against 0.375 for
-// the tile layout above (4 rows per lane).  At M = 16 a byte of B carries
-// four FFMAs, so streaming B at the copy rate needs the FMA pipe about two
-// thirds busy, and the shared-memory pipe is the first to saturate.
+// A block owns an MT x 256 tile of C.  Each stage of its TMA ring carries
+// both operands of DO_TKB k-steps: the DO_TKB x 256 panel of B ([k][n]) and
+// the MT x DO_TKB panel of A ([m][k], rows past M zero-filled by the copy),
+// so the K loop has no block barrier and no global load of its own.  Needs
+// A and B 16-byte aligned with lda % 4 == 0 and ldb % 4 == 0.
 //
-// Stages carry both operands (B panel [k][n], A panel [m][k]) as in the tile
-// variant.  After the K loop the k groups' partial tiles are summed in a
-// fixed order in shared memory, then across the cluster.
+// The four warps split the tile into RG row groups and every stage's k-steps
+// into KG = 4/RG interleaved k groups.  A lane owns the MT/RG rows of its
+// row group and eight columns (lane*4 + {0..3} and 128 + lane*4 + {0..3}):
+// an (MT/RG) x 8 outer product per k.  Per k a lane loads 8 floats of B (two
+// 128-bit loads) and MT/RG broadcast floats of A, so shared memory delivers
+// (MT/RG + 8) floats per lane for 8*MT/RG FFMAs: 0.25 wavefronts per FFMA
+// at MT/RG = 8, against 0.375 with 4 rows per lane.  At M = 16 a byte of B
+// carries four FFMAs, so streaming B at the copy rate needs the FMA pipe
+// about two thirds busy, and with 4 rows per lane the shared-memory pipe
+// saturated first.
+//
+// After the K loop the k groups' partial tiles are summed in a fixed order
+// in shared memory, then across the cluster.
 constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32, DO_TKB = 16;
 #ifndef DECODE_DO_STAGES
 #define DECODE_DO_STAGES 2
@@ -884,11 +692,8 @@ cudaError_t launch_tma(const GemmArgs &g) {
 #ifndef DECODE_DW
 #define DECODE_DW 8
 #endif
-#ifndef DECODE_M16
-#define DECODE_M16 1     // 1: outer-product kernel with two row groups, 0: tile kernel
-#endif
-#ifndef DECODE_TILE_MIN_M
-#define DECODE_TILE_MIN_M 5
+#ifndef DECODE_OUTER_MIN_M
+#define DECODE_OUTER_MIN_M 5
 #endif
 #ifndef DECODE_STAGES
 #define DECODE_STAGES 3
@@ -987,58 +792,14 @@ cudaError_t launch_outer(const GemmArgs &g) {
 }
 
 template <int MT>
-cudaError_t launch_tile(const GemmArgs &g) {
-    using L = DtCfg<MT>;
-    alignas(64) CUtensorMap tmB, tmA;
-    if (!encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, DT_COLS, DT_TKB, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    if (!encode_tma_2d(g.encode, &tmA, g.A, g.K, g.M, g.lda, DT_TKB, MT, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    auto kern = decode_tile_kernel<MT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
-    if (e != cudaSuccess) return e;
-    int ksmax = 8;
-    if (DT_KSMAX > 8) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess)
-            ksmax = DT_KSMAX;
-        else
-            (void)cudaGetLastError();
-    }
-    const int64_t ncb = (g.N + DT_COLS - 1) / DT_COLS;
-    if (ncb > 65535) return cudaErrorInvalidConfiguration;
-
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(DT_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = L::BYTES;
-    cfg.stream = g.stream;
-    static std::atomic<int> cache[64][17];
-    const int ks = choose_cluster(kern, g.K, ncb, ksmax, DT_TKB, cfg, cache);
-    int64_t kslice = (g.K + ks - 1) / ks;
-    kslice = (kslice + DT_TKB - 1) / DT_TKB * DT_TKB;
-
-    cfg.gridDim = dim3((unsigned)ks, (unsigned)ncb, 1);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)ks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmB, tmA, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha,
-                              g.beta, g.C, g.ldc, kslice, g.err, g.wait_ns);
-}
-
-template <int MT>
 cudaError_t launch_vec(const GemmArgs &g) {
     if constexpr (MT >= 8) {
-        if (g.M >= DECODE_TILE_MIN_M && ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) &&
+        if (g.M >= DECODE_OUTER_MIN_M && ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) &&
             (g.ldb % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.A) & 15) == 0) && (g.lda % 4 == 0)) {
             if constexpr (MT <= 8)
                 return launch_outer<MT, 1>(g);
-            else if constexpr (DECODE_M16 == 1)
-                return launch_outer<MT, 2>(g);
             else
-                return launch_tile<MT>(g);
+                return launch_outer<MT, 2>(g);
         }
     }
     const bool vec = ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) && (g.ldb % 4 == 0);
