@@ -85,6 +85,15 @@ class Oracle:
             _i64p, ctypes.c_int64, _f32p, ctypes.c_int64, ctypes.c_int]
         self.lib.oracle_max_threads.restype = ctypes.c_int
         self.lib.oracle_max_threads.argtypes = []
+        self.lib.oracle_round_tf32.restype = None
+        self.lib.oracle_round_tf32.argtypes = [_f32p, _f32p, ctypes.c_int64]
+
+    def round_tf32(self, x: np.ndarray) -> np.ndarray:
+        """x rounded to TF32 (nearest, ties away from zero) as a new float32 array."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty_like(x)
+        self.lib.oracle_round_tf32(_ptr(x.reshape(-1)), _ptr(out.reshape(-1)), x.size)
+        return out
 
     def max_threads(self) -> int:
         return int(self.lib.oracle_max_threads())
@@ -130,6 +139,18 @@ def default() -> Oracle:
     return _default
 
 
-def sgemm(A, B, C0=None, alpha=1.0, beta=0.0, rows=None, threads=0):
-    """alpha*A@B + beta*C0 from the default oracle build (see ``Oracle.sgemm``)."""
+def sgemm(A, B, C0=None, alpha=1.0, beta=0.0, rows=None, threads=0, inputs="fp32"):
+    """alpha*A@B + beta*C0 from the default oracle build (see ``Oracle.sgemm``).
+
+    ``inputs="tf32"`` gives the reduced-precision product: A and B are rounded
+    to TF32 first (``round_tf32``), C0 is not."""
+    if inputs == "tf32":
+        A, B = round_tf32(A), round_tf32(B)
+    elif inputs != "fp32":
+        raise ValueError(f"unknown input precision {inputs!r}")
     return default().sgemm(A, B, C0, alpha=alpha, beta=beta, rows=rows, threads=threads)
+
+
+def round_tf32(x):
+    """x rounded to TF32, nearest with ties away from zero (see ``oracle_round_tf32``)."""
+    return default().round_tf32(x)

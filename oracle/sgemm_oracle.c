@@ -30,9 +30,15 @@
  *
  * The loops run in i-k-j order: one double accumulator row per output row,
  * so each S[i][j] is still summed in ascending k.  OpenMP splits the rows.
+ *
+ * The reduced-precision product (the library's sgemm_tf32) is defined as the
+ * same sum over operands first rounded to TF32 by oracle_round_tf32 below;
+ * the caller rounds A and B and passes the rounded copies to the functions
+ * above (C0 is not rounded).
  */
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -131,4 +137,29 @@ int oracle_sgemm(int64_t M, int64_t N, int64_t K, float alpha,
                                rows, M, out, ldo, nthreads);
     free(rows);
     return rc;
+}
+
+/*
+ * TF32 keeps FP32's sign bit, its 8-bit exponent and the top 10 of its 23
+ * stored mantissa bits.  out[i] = x[i] rounded to the nearest TF32 value,
+ * ties away from zero.  On the bit pattern: add half the weight of the 13
+ * dropped bits (0x1000) to the magnitude, then clear those 13 bits.  A carry
+ * out of the mantissa moves the value to the next binade, and past the
+ * largest finite TF32 value to infinity, as any round-to-nearest does.
+ * Infinities are unchanged; a NaN stays a NaN (its quiet bit is set, so that
+ * clearing the low bits cannot turn it into an infinity).
+ */
+void oracle_round_tf32(const float *x, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t u;
+        memcpy(&u, &x[i], sizeof u);
+        if ((u & 0x7f800000u) == 0x7f800000u) {
+            if (u & 0x007fffffu)
+                u |= 0x00400000u;
+        } else {
+            u = (u + 0x1000u) & 0xffffe000u;
+        }
+        memcpy(&out[i], &u, sizeof u);
+    }
 }

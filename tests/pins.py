@@ -195,6 +195,65 @@ def pin_row_subset(orc):
     assert np.array_equal(orc.sgemm(A, B, C0, alpha=1.0, beta=0.5, rows=rows), full[rows])
 
 
+def _f32(bits):
+    return np.array([bits], dtype=np.uint32).view(np.float32)[0]
+
+
+def pin_tf32_exact_cases(orc):
+    """TF32 rounding (10 stored mantissa bits, nearest, ties away from zero) on
+    hand-computed cases: values already in TF32, values just below / at / just
+    above a tie, a tie whose even neighbour is the lower one, a carry into the
+    next binade, overflow past the largest TF32 value, signed zeros and the
+    special values."""
+    u = 2.0 ** -23
+    cases = [
+        (1.0, 1.0),
+        (1.0 + 2.0 ** -10, 1.0 + 2.0 ** -10),                 # representable
+        (1.0 + 2.0 ** -11, 1.0 + 2.0 ** -10),                 # tie: away from zero
+        (1.0 + 2.0 ** -11 - u, 1.0),                          # just below the tie
+        (1.0 + 2.0 ** -11 + u, 1.0 + 2.0 ** -10),             # just above the tie
+        (-(1.0 + 2.0 ** -11), -(1.0 + 2.0 ** -10)),           # tie, negative: away
+        (1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -9),              # tie; the even neighbour is below
+        (2.0 - u, 2.0),                                       # carry into the next binade
+        (3.0 * 2.0 ** -130, 3.0 * 2.0 ** -130),               # subnormal, representable
+        ((2.0 - 2.0 ** -10) * 2.0 ** 127, (2.0 - 2.0 ** -10) * 2.0 ** 127),   # largest TF32
+        (float(np.finfo(np.float32).max), np.inf),            # above it: overflow
+        (np.inf, np.inf), (-np.inf, -np.inf),
+    ]
+    x = np.array([c[0] for c in cases], dtype=np.float32)
+    want = np.array([c[1] for c in cases], dtype=np.float32)
+    got = orc.round_tf32(x)
+    assert np.array_equal(got, want), (x, got, want)
+    z = orc.round_tf32(np.array([0.0, -0.0], dtype=np.float32))
+    assert z[0] == 0 and not np.signbit(z[0]) and z[1] == 0 and np.signbit(z[1])
+    nan = orc.round_tf32(np.array([np.nan, _f32(0x7f800001), _f32(0xff800001)], dtype=np.float32))
+    assert np.all(np.isnan(nan))
+
+
+def pin_tf32_nearest(orc):
+    """On random normal floats of every exponent the result is a TF32 value,
+    it is one of the two TF32 values around x (x cut toward zero to 10 stored
+    bits, and that plus one TF32 step away from zero), it is at least as close
+    to x as the other one in exact fp64 arithmetic, and on a tie it is the one
+    farther from zero."""
+    rng = _rng(97)
+    bits = rng.integers(0x00800000, 0x7f000000, size=200000, dtype=np.uint32)
+    bits |= rng.integers(0, 2, size=bits.size, dtype=np.uint32) << 31
+    bits[:2000] = (bits[:2000] & 0xffffe000) | 0x1000          # exact ties
+    x = bits.view(np.float32)
+    r = orc.round_tf32(x)
+    assert np.all((r.view(np.uint32) & 0x1fff) == 0), "result has more than 10 stored bits"
+    cut = (bits & 0xffffe000).view(np.float32).astype(np.float64)      # toward zero
+    e = np.floor(np.log2(np.abs(cut)))
+    up = cut + np.sign(cut) * np.exp2(e - 10)                          # one TF32 step away
+    xd, rd = x.astype(np.float64), r.astype(np.float64)
+    assert np.all((rd == cut) | (rd == up)), "not a neighbour of x"
+    d_r, d_o = np.abs(xd - rd), np.abs(xd - np.where(rd == cut, up, cut))
+    assert np.all(d_r <= d_o), "not the nearest neighbour"
+    tie = d_r == d_o
+    assert tie[:2000].all() and np.all(np.abs(rd[tie]) > np.abs(xd[tie])), "tie not away from zero"
+
+
 ALL_PINS = [pin_small_int_exact, pin_exact_rational, pin_identity, pin_permutation,
             pin_rank1, pin_transpose, pin_freivalds, pin_alpha_beta, pin_ld_gaps,
-            pin_row_subset]
+            pin_row_subset, pin_tf32_exact_cases, pin_tf32_nearest]

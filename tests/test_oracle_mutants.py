@@ -40,6 +40,10 @@ MUTANTS = [
      "const int use_ab = (K > 0);"),
     ("column_shift", "acc[j] += a * (double)brow[j];",
      "acc[j] += a * (double)brow[(j + 1) % N];"),
+    ("tf32_truncates", "u = (u + 0x1000u) & 0xffffe000u;", "u = u & 0xffffe000u;"),
+    ("tf32_ties_even", "u = (u + 0x1000u) & 0xffffe000u;",
+     "u = (u + 0x0fffu + ((u >> 13) & 1u)) & 0xffffe000u;"),
+    ("tf32_keeps_11_bits", "u = (u + 0x1000u) & 0xffffe000u;", "u = (u + 0x0800u) & 0xfffff000u;"),
 ]
 
 CHILD = textwrap.dedent("""
