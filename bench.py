@@ -322,6 +322,12 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3):
                                 "tensor_TFLOP/s": 3 * useful, "tf32_peak": tf32_peak,
                                 "frac_tf32_peak": 3 * useful / tf32_peak,
                                 "frac_useful_ceiling": useful / (tf32_peak / 3)}
+    # reduced-precision path: operands rounded to TF32, one MMA per k-step
+    per, st, kn, pe = bench_shape(8192, 8192, 8192, 1.0, tensor_cores=sg.MODE_TF32)
+    tfl = 2 * 8192**3 / (per * 1e-3) / 1e12
+    out["sgemm_8192_tf32"] = {"shape": [8192, 8192, 8192], "kernel": kn, "ms": per, "ms_eager": pe,
+                              "status": st, "TFLOP/s": tfl, "tf32_peak": tf32_peak,
+                              "frac_tf32_peak": tfl / tf32_peak}
     return out
 
 

@@ -15,8 +15,9 @@ import os
 
 from .build import LIBRARY, build  # noqa: F401  (build is part of the public API)
 
-__all__ = ["sgemm", "sgemm_3xtf32", "sgemm_ptr", "status", "select_kernel", "force_kernel",
-           "set_wait_limit", "selftest_wait", "release_workspaces", "status_string", "version", "SgemmError", "lib"]
+__all__ = ["sgemm", "sgemm_3xtf32", "sgemm_tf32", "sgemm_ptr", "status", "select_kernel",
+           "force_kernel", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
+           "version", "SgemmError", "lib"]
 
 OK = 0
 ERR_BAD_DIM, ERR_BAD_LD, ERR_NULL_PTR, ERR_ALIAS = -1, -2, -3, -4
@@ -24,10 +25,24 @@ ERR_CUDA, ERR_DEVICE, ERR_TIMEOUT, ERR_BAD_ARG = -5, -6, -7, -8
 ERR_TOO_LARGE, ERR_CAPTURE = -9, -10
 
 KERNEL_AUTO, KERNEL_NONE, KERNEL_SCALE_C, KERNEL_FFMA_TMA = 0, 1, 2, 3
-KERNEL_FFMA_GENERIC, KERNEL_DECODE, KERNEL_TF32X3 = 4, 5, 6
+KERNEL_FFMA_GENERIC, KERNEL_DECODE, KERNEL_TF32X3, KERNEL_TF32 = 4, 5, 6, 7
 KERNEL_NAMES = {KERNEL_NONE: "none", KERNEL_SCALE_C: "scale_c", KERNEL_FFMA_TMA: "ffma_tma",
                 KERNEL_FFMA_GENERIC: "ffma_generic", KERNEL_DECODE: "decode",
-                KERNEL_TF32X3: "tf32x3"}
+                KERNEL_TF32X3: "tf32x3", KERNEL_TF32: "tf32"}
+# arithmetic of a call (sgemm, sgemm_3xtf32, sgemm_tf32)
+MODE_FP32, MODE_3XTF32, MODE_TF32 = 0, 1, 2
+_ENTRY = {MODE_FP32: "sgemm", MODE_3XTF32: "sgemm_3xtf32", MODE_TF32: "sgemm_tf32"}
+
+
+def _mode(tensor_cores) -> int:
+    """False/True (FP32 / 3xTF32) or one of the MODE_* values."""
+    if tensor_cores is True:
+        return MODE_3XTF32
+    if tensor_cores is False or tensor_cores is None:
+        return MODE_FP32
+    if tensor_cores in _ENTRY:
+        return int(tensor_cores)
+    raise ValueError(f"unknown arithmetic mode {tensor_cores!r}")
 
 
 class SgemmError(RuntimeError):
@@ -51,7 +66,7 @@ def lib() -> ctypes.CDLL:
                 f"CUDA library {LIBRARY} is not built; run "
                 "`python -m dense_fp32_matrix_row_gb300.build` (there is no CPU fallback)")
         L = ctypes.CDLL(LIBRARY)
-        for name in ("sgemm", "sgemm_3xtf32"):
+        for name in ("sgemm", "sgemm_3xtf32", "sgemm_tf32"):
             getattr(L, name).argtypes = _GEMM_ARGS
             getattr(L, name).restype = ctypes.c_int
         L.sgemm_select_kernel.argtypes = _GEMM_ARGS[:-1] + [ctypes.c_int]
@@ -114,8 +129,9 @@ def _check_operand(t, name):
 
 
 def sgemm_ptr(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0, tensor_cores=False) -> int:
-    """Raw C-ABI call on device pointers; returns the status code."""
-    fn = lib().sgemm_3xtf32 if tensor_cores else lib().sgemm
+    """Raw C-ABI call on device pointers; returns the status code.
+    ``tensor_cores``: False (sgemm), True (sgemm_3xtf32) or a MODE_* value."""
+    fn = getattr(lib(), _ENTRY[_mode(tensor_cores)])
     return int(fn(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream))
 
 
@@ -126,7 +142,9 @@ def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
     A is (M, K), B (K, N), C (M, N); each may be a row-strided view (row
     stride >= row length).  Enqueued on ``stream`` (default: the current torch
     stream of C's device); returns without waiting.  ``tensor_cores`` selects
-    the 3xTF32 tcgen05 path.  Raises SgemmError on a rejected call.
+    the arithmetic: False (FP32 FFMA), True (3xTF32 tcgen05 path) or a MODE_*
+    value (MODE_TF32: the reduced-precision 1xTF32 path).  Raises SgemmError
+    on a rejected call.
     """
     for t, n in ((A, "A"), (B, "B"), (C, "C")):
         _check_operand(t, n)
@@ -139,12 +157,18 @@ def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
                    _ld(B), float(beta), C.data_ptr() or None, _ld(C),
                    _stream_handle(stream, dev), tensor_cores)
     if rc != OK:
-        raise SgemmError(rc, "sgemm_3xtf32" if tensor_cores else "sgemm")
+        raise SgemmError(rc, _ENTRY[_mode(tensor_cores)])
 
 
 def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
     """``sgemm`` on the 3xTF32 tensor-core path."""
     sgemm(A, B, C, alpha, beta, stream, tensor_cores=True)
+
+
+def sgemm_tf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
+    """``sgemm`` on the reduced-precision 1xTF32 tensor-core path: A and B are
+    rounded to TF32 first (see include/sgemm_gb300.h for the contract)."""
+    sgemm(A, B, C, alpha, beta, stream, tensor_cores=MODE_TF32)
 
 
 def status(stream=None) -> int:
@@ -159,7 +183,7 @@ def select_kernel(M, N, K, alpha=1.0, A=16, lda=None, B=16, ldb=None, beta=0.0, 
     ldb = N if ldb is None else ldb
     ldc = N if ldc is None else ldc
     return int(lib().sgemm_select_kernel(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
-                                         1 if tensor_cores else 0))
+                                         _mode(tensor_cores)))
 
 
 def force_kernel(kernel_id: int) -> int:

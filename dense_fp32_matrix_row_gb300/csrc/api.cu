@@ -169,13 +169,16 @@ bool kernel_can_run(int id, int64_t M, int64_t N, int64_t K, const float *A, int
         case SGEMM_KERNEL_FFMA_TMA: return tma_ok(M, N, K, A, lda, B, ldb);
         case SGEMM_KERNEL_FFMA_GENERIC: return (M + 63) / 64 <= 65535;
         case SGEMM_KERNEL_DECODE: return M <= 16 && (N + 127) / 128 <= 65535;
-        case SGEMM_KERNEL_TF32X3: return tf32x3_can_run(M, N, K);
+        case SGEMM_KERNEL_TF32X3:
+        case SGEMM_KERNEL_TF32: return tf32x3_can_run(M, N, K);
         default: return false;
     }
 }
 
 int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
-           const float *B, int64_t ldb, float beta, const float *C, int64_t ldc, bool tensor) {
+           const float *B, int64_t ldb, float beta, const float *C, int64_t ldc, int mode) {
+    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32)
+        return SGEMM_ERR_BAD_ARG;
     bool uses_ab = false;
     const int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &uses_ab);
     if (rc != SGEMM_OK) return rc;
@@ -186,8 +189,10 @@ int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t
         return forced;
     // The tensor-core tile is 128 rows tall; skinny products stay on the
     // (FP32-exact) decode kernel.
-    if (tensor && M > 16 && kernel_can_run(SGEMM_KERNEL_TF32X3, M, N, K, A, lda, B, ldb))
-        return SGEMM_KERNEL_TF32X3;
+    if (mode != SGEMM_MODE_FP32 && M > 16) {
+        const int tc = mode == SGEMM_MODE_3XTF32 ? SGEMM_KERNEL_TF32X3 : SGEMM_KERNEL_TF32;
+        if (kernel_can_run(tc, M, N, K, A, lda, B, ldb)) return tc;
+    }
     if (M <= 16 && kernel_can_run(SGEMM_KERNEL_DECODE, M, N, K, A, lda, B, ldb))
         return SGEMM_KERNEL_DECODE;
     if (tma_ok(M, N, K, A, lda, B, ldb)) return SGEMM_KERNEL_FFMA_TMA;
@@ -197,8 +202,8 @@ int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t
 }
 
 int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda, const float *B,
-        int64_t ldb, float beta, float *C, int64_t ldc, void *stream, bool tensor) {
-    const int kid = choose(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tensor);
+        int64_t ldb, float beta, float *C, int64_t ldc, void *stream, int mode) {
+    const int kid = choose(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode);
     if (kid < 0) return kid;
     if (kid == SGEMM_KERNEL_NONE) return SGEMM_OK;
     DeviceState *st = nullptr;
@@ -228,11 +233,14 @@ int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t ld
             e = launch_ffma_tma(g, ws, nf);
             break;
         }
-        case SGEMM_KERNEL_TF32X3: {
+        case SGEMM_KERNEL_TF32X3:
+        case SGEMM_KERNEL_TF32: {
+            const int terms = kid == SGEMM_KERNEL_TF32X3 ? 3 : 1;
             float *ws = nullptr;
-            const int rc = workspace(tf32x3_workspace_floats(M, N, K) * sizeof(float), g.stream, &ws);
+            const int rc =
+                workspace(tf32_workspace_floats(M, N, K, terms) * sizeof(float), g.stream, &ws);
             if (rc != SGEMM_OK) return rc;
-            e = launch_tf32x3(g, ws);
+            e = launch_tf32(g, ws, terms);
             break;
         }
         default: return SGEMM_ERR_BAD_ARG;
@@ -294,12 +302,17 @@ extern "C" {
 
 int sgemm(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
           const float *B, int64_t ldb, float beta, float *C, int64_t ldc, void *stream) {
-    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, false);
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, SGEMM_MODE_FP32);
 }
 
 int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
                  const float *B, int64_t ldb, float beta, float *C, int64_t ldc, void *stream) {
-    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, true);
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, SGEMM_MODE_3XTF32);
+}
+
+int sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+               const float *B, int64_t ldb, float beta, float *C, int64_t ldc, void *stream) {
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, SGEMM_MODE_TF32);
 }
 
 int sgemm_status(void *stream) {
@@ -342,13 +355,13 @@ const char *sgemm_status_string(int status) {
 
 int sgemm_select_kernel(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
                         const float *B, int64_t ldb, float beta, const float *C, int64_t ldc,
-                        int tensor_cores) {
-    return choose(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, tensor_cores != 0);
+                        int mode) {
+    return choose(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode);
 }
 
 int sgemm_force_kernel(int id) {
     if (id != SGEMM_KERNEL_AUTO && id != SGEMM_KERNEL_FFMA_TMA && id != SGEMM_KERNEL_FFMA_GENERIC &&
-        id != SGEMM_KERNEL_DECODE && id != SGEMM_KERNEL_TF32X3)
+        id != SGEMM_KERNEL_DECODE && id != SGEMM_KERNEL_TF32X3 && id != SGEMM_KERNEL_TF32)
         return SGEMM_ERR_BAD_ARG;
     return g_force.exchange(id);
 }

@@ -57,19 +57,23 @@ int64_t ffma_tma_max_m();
 cudaError_t launch_transpose(int64_t M, int64_t K, const float *A, int64_t lda, float *At,
                              int64_t ldt, cudaStream_t stream, unsigned *zero = nullptr,
                              int nzero = 0);
-// TF32 hi/lo split of B (K x N) written transposed: hi[n*ldo + k], lo[n*ldo + k].
+// TF32 hi/lo split of B (K x N) written transposed: hi[n*ldo + k], lo[n*ldo + k]
+// (lo == nullptr: the rounded hi part only).
 cudaError_t launch_transpose_split(int64_t K, int64_t N, const float *B, int64_t ldb, float *hi,
                                    float *lo, int64_t ldo, cudaStream_t stream);
-// TF32 hi/lo split of X (R x Cc) in place of layout: hi[r*ldo + c], lo[r*ldo + c].
+// TF32 hi/lo split of X (R x Cc) in place of layout: hi[r*ldo + c], lo[r*ldo + c]
+// (lo == nullptr: the rounded hi part only).
 cudaError_t launch_split_rows(int64_t R, int64_t Cc, const float *X, int64_t ldx, float *hi,
                               float *lo, int64_t ldo, cudaStream_t stream);
 cudaError_t launch_decode(const GemmArgs &g);
 cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream);
-// 3xTF32 tensor-core kernel: splits A and B into TF32 hi/lo parts in
-// `workspace` (tf32x3_workspace_floats(M, N, K) floats), then runs the
-// tcgen05 MMA kernel.
-cudaError_t launch_tf32x3(const GemmArgs &g, float *workspace);
-size_t tf32x3_workspace_floats(int64_t M, int64_t N, int64_t K);
+// TF32 tensor-core kernels.  terms == 3 (3xTF32): splits A and B into TF32
+// hi/lo parts in `workspace`, then accumulates hi*lo + lo*hi + hi*hi with
+// tcgen05 MMAs.  terms == 1 (1xTF32): rounds A and B to TF32 (the hi parts
+// only) and accumulates hi*hi.  The workspace holds
+// tf32_workspace_floats(M, N, K, terms) floats.
+cudaError_t launch_tf32(const GemmArgs &g, float *workspace, int terms);
+size_t tf32_workspace_floats(int64_t M, int64_t N, int64_t K, int terms);
 bool tf32x3_can_run(int64_t M, int64_t N, int64_t K);
 // Fills g.err, g.wait_ns, g.sm_count and g.encode for the current device
 // (setting the device up on first use); returns an SGEMM_* status.

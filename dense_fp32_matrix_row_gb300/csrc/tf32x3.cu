@@ -32,7 +32,7 @@
 namespace sgemm_gb300 {
 namespace {
 
-constexpr int TBM = 128, TBN = 256, TBK = 16, TSTG = 4;
+constexpr int TBM = 128, TBN = 256, TBK = 16;
 constexpr int KC_TILES = 4;                     // k-tiles per accumulation chunk (64 k)
 constexpr int EPI_WARPS = 8;                    // two warpgroups: 32 rows x 128 columns each
 constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
@@ -41,9 +41,19 @@ constexpr int EPI_COLS = TBN / (EPI_WARPS / 4); // columns per epilogue thread
 constexpr int RASTER_GROUP = 16;                // M tiles walked together (L2 reuse)
 constexpr uint32_t A_TILE = TBM * TBK * 4;                 // 8 KB
 constexpr uint32_t B_TILE = TBN * TBK * 4;                 // 16 KB
-constexpr uint32_t STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;  // 48 KB
 constexpr uint32_t TMEM_COLS = 2 * TBN;                    // two 128 x 256 FP32 accumulators
-constexpr size_t SMEM = 1024 + (size_t)TSTG * STAGE_BYTES + 256;
+
+// Per-stage layout: the A parts, then the B parts (hi, then lo for 3 terms).
+// 3 terms: 48 KB stages, 4 deep; 1 term: 24 KB stages, 8 deep (192 KB both).
+template <int TERMS>
+struct TfCfg {
+    static constexpr int PARTS = TERMS == 3 ? 2 : 1;
+    static constexpr uint32_t STAGE_BYTES = PARTS * (A_TILE + B_TILE);
+    static constexpr int TSTG = TERMS == 3 ? 4 : 8;
+    static constexpr size_t SMEM = 1024 + (size_t)TSTG * STAGE_BYTES + 256;
+    static_assert(TERMS == 1 || TERMS == 3, "1xTF32 or 3xTF32");
+    static_assert(SMEM <= 227 * 1024, "shared memory per block");
+};
 constexpr uint64_t DRAIN_NS = 1000000000ull;
 static_assert(TBK * 4 == 64, "rows of a K slice fill exactly one 64-byte swizzle span");
 static_assert(A_TILE % 1024 == 0 && B_TILE % 1024 == 0, "tiles keep 1024-byte alignment");
@@ -113,11 +123,15 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 // thread therefore restarts the accumulator every KC_TILES k-tiles, in two
 // alternating tensor-memory buffers, and the epilogue warps add each chunk
 // into FP32 registers (round to nearest) while the next chunk is computed.
+template <int TERMS>
 __global__ void __launch_bounds__(THREADS, 1)
-tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
-              const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
-              int M, int N, int K, float alpha, float beta, float *__restrict__ C, int64_t ldc,
-              int c_vec4, unsigned *err, uint64_t wait_ns) {
+tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
+                const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
+                int M, int N, int K, float alpha, float beta, float *__restrict__ C, int64_t ldc,
+                int c_vec4, unsigned *err, uint64_t wait_ns) {
+    using L = TfCfg<TERMS>;
+    constexpr int TSTG = L::TSTG;
+    constexpr uint32_t STAGE_BYTES = L::STAGE_BYTES;
     extern __shared__ unsigned char smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
     unsigned char *ring = reinterpret_cast<unsigned char *>(base);
@@ -142,7 +156,8 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__
     const int ktiles = (K + TBK - 1) / TBK;
     const int nchunks = (ktiles + KC_TILES - 1) / KC_TILES;
     auto stage_ptr = [&](int s, int which) -> uint32_t {   // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
-        const uint32_t off = which < 2 ? which * A_TILE : 2 * A_TILE + (which - 2) * B_TILE;
+        constexpr int P = L::PARTS;
+        const uint32_t off = which < 2 ? which * A_TILE : P * A_TILE + (which - 2) * B_TILE;
         return smem_u32(ring + (size_t)s * STAGE_BYTES + off);
     };
 
@@ -174,9 +189,11 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__
     if (warp == PRODUCER_WARP) {
         if (lane == 0) {
             tma_prefetch_desc(&tmAhi);
-            tma_prefetch_desc(&tmAlo);
             tma_prefetch_desc(&tmBhi);
-            tma_prefetch_desc(&tmBlo);
+            if (TERMS == 3) {
+                tma_prefetch_desc(&tmAlo);
+                tma_prefetch_desc(&tmBlo);
+            }
             int kt = 0;
             for (; kt < ktiles; ++kt) {
                 const int s = kt % TSTG;
@@ -185,9 +202,11 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, STAGE_BYTES);
                 tma_load_2d(stage_ptr(s, 0), &tmAhi, fb, kt * TBK, m0);
-                tma_load_2d(stage_ptr(s, 1), &tmAlo, fb, kt * TBK, m0);
                 tma_load_2d(stage_ptr(s, 2), &tmBhi, fb, kt * TBK, n0);
-                tma_load_2d(stage_ptr(s, 3), &tmBlo, fb, kt * TBK, n0);
+                if (TERMS == 3) {
+                    tma_load_2d(stage_ptr(s, 1), &tmAlo, fb, kt * TBK, m0);
+                    tma_load_2d(stage_ptr(s, 3), &tmBlo, fb, kt * TBK, n0);
+                }
             }
             if (kt < ktiles) {
                 record_error(err, kErrWaitTimeout);
@@ -221,13 +240,17 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__
                     for (int kk = 0; kk < TBK / 8; ++kk) {
                         const uint32_t koff = kk * 32;   // 8 TF32 = 32 bytes along K
                         const uint64_t ahi = smem_desc_sw64(stage_ptr(s, 0) + koff);
-                        const uint64_t alo = smem_desc_sw64(stage_ptr(s, 1) + koff);
                         const uint64_t bhi = smem_desc_sw64(stage_ptr(s, 2) + koff);
-                        const uint64_t blo = smem_desc_sw64(stage_ptr(s, 3) + koff);
                         const uint32_t acc_in = (kt != c * KC_TILES || kk != 0) ? 1u : 0u;
-                        tc_mma_tf32(d, ahi, blo, acc_in);
-                        tc_mma_tf32(d, alo, bhi, 1u);
-                        tc_mma_tf32(d, ahi, bhi, 1u);
+                        if (TERMS == 3) {
+                            const uint64_t alo = smem_desc_sw64(stage_ptr(s, 1) + koff);
+                            const uint64_t blo = smem_desc_sw64(stage_ptr(s, 3) + koff);
+                            tc_mma_tf32(d, ahi, blo, acc_in);
+                            tc_mma_tf32(d, alo, bhi, 1u);
+                            tc_mma_tf32(d, ahi, bhi, 1u);
+                        } else {
+                            tc_mma_tf32(d, ahi, bhi, acc_in);
+                        }
                     }
                     issued_any = true;
                     tc_commit(smem_u32(&empty[s]));   // the stage is free once these MMAs are done
@@ -323,28 +346,20 @@ tf32x3_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__
     }
 }
 
-}  // namespace
 
-int64_t tf32x3_ld(int64_t K) { return (K + 3) / 4 * 4; }
+int64_t tf32_ld(int64_t K) { return (K + 3) / 4 * 4; }
 
-size_t tf32x3_workspace_floats(int64_t M, int64_t N, int64_t K) {
-    const int64_t ldk = tf32x3_ld(K);
-    const int64_t a = (M * ldk + 63) / 64 * 64, b = (N * ldk + 63) / 64 * 64;
-    return (size_t)(2 * a + 2 * b);
-}
-
-bool tf32x3_can_run(int64_t M, int64_t N, int64_t K) {
-    const int64_t lim = int64_t(1) << 31;
-    return M < lim && N < lim && K < lim && ((M + TBM - 1) / TBM) * ((N + TBN - 1) / TBN) <= 0x7fffffff &&
-           (K + 31) / 32 <= 65535;
-}
-
-cudaError_t launch_tf32x3(const GemmArgs &g, float *ws) {
-    const int64_t ldk = tf32x3_ld(g.K);
+template <int TERMS>
+cudaError_t launch_terms(const GemmArgs &g, float *ws) {
+    using L = TfCfg<TERMS>;
+    const int64_t ldk = tf32_ld(g.K);
     const int64_t asz = (g.M * ldk + 63) / 64 * 64, bsz = (g.N * ldk + 63) / 64 * 64;
-    float *ahi = ws, *alo = ws + asz, *bhi = ws + 2 * asz, *blo = ws + 2 * asz + bsz;
+    // workspace: A_hi, B_hi, then (3 terms) A_lo, B_lo
+    float *ahi = ws, *bhi = ws + asz;
+    float *alo = TERMS == 3 ? ws + asz + bsz : nullptr;
+    float *blo = TERMS == 3 ? ws + 2 * asz + bsz : nullptr;
 
-    // split A (rows stay rows), split + transpose B
+    // round / split A (rows stay rows), round / split + transpose B
     cudaError_t e = launch_split_rows(g.M, g.K, g.A, g.lda, ahi, alo, ldk, g.stream);
     if (e != cudaSuccess) return e;
     e = launch_transpose_split(g.K, g.N, g.B, g.ldb, bhi, blo, ldk, g.stream);
@@ -353,20 +368,47 @@ cudaError_t launch_tf32x3(const GemmArgs &g, float *ws) {
     alignas(64) CUtensorMap tAhi, tAlo, tBhi, tBlo;
     const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
     if (!encode_tma_2d(g.encode, &tAhi, ahi, g.K, g.M, ldk, TBK, TBM, sw) ||
-        !encode_tma_2d(g.encode, &tAlo, alo, g.K, g.M, ldk, TBK, TBM, sw) ||
-        !encode_tma_2d(g.encode, &tBhi, bhi, g.K, g.N, ldk, TBK, TBN, sw) ||
-        !encode_tma_2d(g.encode, &tBlo, blo, g.K, g.N, ldk, TBK, TBN, sw))
+        !encode_tma_2d(g.encode, &tBhi, bhi, g.K, g.N, ldk, TBK, TBN, sw))
         return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM);
+    if (TERMS == 3) {
+        if (!encode_tma_2d(g.encode, &tAlo, alo, g.K, g.M, ldk, TBK, TBM, sw) ||
+            !encode_tma_2d(g.encode, &tBlo, blo, g.K, g.N, ldk, TBK, TBN, sw))
+            return cudaErrorInvalidValue;
+    } else {
+        tAlo = tAhi;   // never read
+        tBlo = tBhi;
+    }
+    e = cudaFuncSetAttribute(tf32_mma_kernel<TERMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)L::SMEM);
     if (e != cudaSuccess) return e;
     const int64_t tiles = ((g.N + TBN - 1) / TBN) * ((g.M + TBM - 1) / TBM);
     if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)tiles);
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
-    tf32x3_kernel<<<grid, THREADS, SMEM, g.stream>>>(tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N,
-                                                     (int)g.K, g.alpha, g.beta, g.C, g.ldc, c_vec4,
-                                                     g.err, g.wait_ns);
+    tf32_mma_kernel<TERMS><<<grid, THREADS, L::SMEM, g.stream>>>(
+        tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N, (int)g.K, g.alpha, g.beta, g.C, g.ldc, c_vec4,
+        g.err, g.wait_ns);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t tf32_workspace_floats(int64_t M, int64_t N, int64_t K, int terms) {
+    const int64_t ldk = tf32_ld(K);
+    const int64_t a = (M * ldk + 63) / 64 * 64, b = (N * ldk + 63) / 64 * 64;
+    return (size_t)((terms == 3 ? 2 : 1) * (a + b));
+}
+
+bool tf32x3_can_run(int64_t M, int64_t N, int64_t K) {
+    const int64_t lim = int64_t(1) << 31;
+    return M < lim && N < lim && K < lim && ((M + TBM - 1) / TBM) * ((N + TBN - 1) / TBN) <= 0x7fffffff &&
+           (K + 31) / 32 <= 65535;
+}
+
+cudaError_t launch_tf32(const GemmArgs &g, float *ws, int terms) {
+    if (terms == 3) return launch_terms<3>(g, ws);
+    if (terms == 1) return launch_terms<1>(g, ws);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace sgemm_gb300

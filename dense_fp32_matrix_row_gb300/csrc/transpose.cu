@@ -2,9 +2,9 @@
 //
 //  * launch_transpose:       At[k][m] = A[m][k] (the FFMA kernel's K-major A);
 //  * launch_transpose_split: hi[n][k] = tf32(B[k][n]), lo[n][k] = tf32(B[k][n] - hi)
-//                            (the 3xTF32 kernel's K-major B halves);
+//                            (the TF32 kernels' K-major B; lo skipped when null);
 //  * launch_split_rows:      hi[r][c] = tf32(X[r][c]), lo[r][c] = tf32(X[r][c] - hi)
-//                            (the 3xTF32 kernel's A halves).
+//                            (the TF32 kernels' A; lo skipped when null).
 //
 // The FFMA kernel reads A as K-major tiles (four consecutive rows in one
 // 128-bit shared load), the layout the pages reach by transposing A on its way
@@ -83,16 +83,17 @@ transpose_tile_kernel(int64_t R, int64_t Cc, const float *__restrict__ src, int6
             }
         }
         float *ph = dst_hi + c * ldd + r;
-        float *pl = SPLIT ? dst_lo + c * ldd + r : nullptr;
+        const bool wlo = SPLIT && dst_lo != nullptr;
+        float *pl = wlo ? dst_lo + c * ldd + r : nullptr;
         if (r + 3 < R) {
             *reinterpret_cast<float4 *>(ph) = make_float4(h[0], h[1], h[2], h[3]);
-            if (SPLIT) *reinterpret_cast<float4 *>(pl) = make_float4(l[0], l[1], l[2], l[3]);
+            if (wlo) *reinterpret_cast<float4 *>(pl) = make_float4(l[0], l[1], l[2], l[3]);
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (r + e < R) {
                     ph[e] = h[e];
-                    if (SPLIT) pl[e] = l[e];
+                    if (wlo) pl[e] = l[e];
                 }
             }
         }
@@ -125,16 +126,17 @@ split_rows_kernel(int64_t R, int64_t Cc, const float *__restrict__ X, int64_t ld
                 h[e] = tf32_rna(v[e]);
                 l[e] = tf32_rna(v[e] - h[e]);
             }
-            float *ph = hi + r * ldo + c, *pl = lo + r * ldo + c;
+            float *ph = hi + r * ldo + c;
+            float *pl = lo != nullptr ? lo + r * ldo + c : nullptr;
             if (full) {
                 *reinterpret_cast<float4 *>(ph) = make_float4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<float4 *>(pl) = make_float4(l[0], l[1], l[2], l[3]);
+                if (pl) *reinterpret_cast<float4 *>(pl) = make_float4(l[0], l[1], l[2], l[3]);
             } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     if (c + e < Cc) {
                         ph[e] = h[e];
-                        pl[e] = l[e];
+                        if (pl) pl[e] = l[e];
                     }
             }
         }

@@ -78,6 +78,12 @@ extern "C" {
 #define SGEMM_KERNEL_FFMA_GENERIC  4   /* plain-load tiled FFMA kernel, any alignment */
 #define SGEMM_KERNEL_DECODE        5   /* split-K streaming kernel for M <= 16 */
 #define SGEMM_KERNEL_TF32X3        6   /* 3xTF32 tensor-core kernel (sgemm_3xtf32) */
+#define SGEMM_KERNEL_TF32          7   /* 1xTF32 tensor-core kernel (sgemm_tf32) */
+
+/* Arithmetic of a call, for sgemm_select_kernel's `mode`. */
+#define SGEMM_MODE_FP32    0   /* sgemm() */
+#define SGEMM_MODE_3XTF32  1   /* sgemm_3xtf32() */
+#define SGEMM_MODE_TF32    2   /* sgemm_tf32() */
 
 /*
  * sgemm -- C <- alpha * A @ B + beta * C in FP32 (FFMA) arithmetic.
@@ -128,6 +134,30 @@ int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha,
                  float beta, float *C, int64_t ldc, void *stream);
 
 /*
+ * sgemm_tf32 -- reduced-precision product on the tcgen05 tensor cores
+ * (opt-in; TF32 is named on "CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS",
+ * results-table note).
+ *
+ * Accuracy contract: A and B are first rounded to TF32 (FP32's sign and
+ * exponent, 10 stored mantissa bits; round to nearest, ties away from zero),
+ * and the result is the FP32-accumulated product of the rounded operands,
+ * C = alpha * round(A) @ round(B) + beta * C.  Against that definition the
+ * result meets sgemm()'s FP32 accuracy; against the unrounded product its
+ * error is that of the input rounding, up to 2^-11 relative per operand
+ * (about 1e-5 of K*max|A|*max|B| for random data at K = 4096).  Operands
+ * that are already TF32 values (small integers, for instance) give the same
+ * result as sgemm_3xtf32().  C is not rounded.
+ * The operands are rounded into a workspace first (A as [M][K], B
+ * transposed to [N][K]: (M+N)*round_up(K,4) floats, grown like sgemm()'s),
+ * so any alignment and ld are accepted.  Skinny products (M <= 16) run
+ * sgemm()'s FP32 decode kernel, which is more accurate than the contract.
+ * Arguments, conventions and errors are those of sgemm().
+ */
+int sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha,
+               const float *A, int64_t lda, const float *B, int64_t ldb,
+               float beta, float *C, int64_t ldc, void *stream);
+
+/*
  * sgemm_status -- wait for `stream`, then report and clear the current
  * device's kernel error word.  Returns SGEMM_OK, SGEMM_ERR_TIMEOUT when a
  * kernel's bounded wait ran out since the last call (that kernel skipped its
@@ -141,12 +171,13 @@ const char *sgemm_status_string(int status);
 /*
  * sgemm_select_kernel -- which SGEMM_KERNEL_* sgemm() would run for these
  * arguments (host-only, launches nothing, needs no GPU).  Returns a negative
- * status code for arguments sgemm() would reject.  `tensor_cores` != 0 asks
- * for the choice of sgemm_3xtf32() instead.
+ * status code for arguments sgemm() would reject.  `mode` is one of
+ * SGEMM_MODE_*: the choice of sgemm(), sgemm_3xtf32() or sgemm_tf32();
+ * SGEMM_ERR_BAD_ARG for any other value.
  */
 int sgemm_select_kernel(int64_t M, int64_t N, int64_t K, float alpha,
                         const float *A, int64_t lda, const float *B, int64_t ldb,
-                        float beta, const float *C, int64_t ldc, int tensor_cores);
+                        float beta, const float *C, int64_t ldc, int mode);
 
 /*
  * sgemm_force_kernel -- test hook: make later calls (all host threads) run

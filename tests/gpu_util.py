@@ -121,7 +121,10 @@ def run_checked(sg, A, B, C0, alpha, beta, *, kernel=None, lds=(None, None, None
     assert pc.outside_intact(h), "a write landed outside C's elements (gap or guard)"
     assert pa.unchanged() and pb.unchanged(), "A or B was modified"
     use_ab = alpha != 0.0 and K > 0
-    Cref = oracle.sgemm(A, B, C0 if beta != 0.0 else None, alpha=alpha, beta=beta, rows=rows)
+    # the reduced-precision path is defined on TF32-rounded operands
+    inputs = "tf32" if sg._mode(tensor_cores) == sg.MODE_TF32 else "fp32"
+    Cref = oracle.sgemm(A, B, C0 if beta != 0.0 else None, alpha=alpha, beta=beta, rows=rows,
+                        inputs=inputs)
     got = C if rows is None else C[rows]
     if exact or not use_ab:
         assert np.array_equal(got.view(np.uint32), Cref.view(np.uint32)) or np.array_equal(got, Cref), \

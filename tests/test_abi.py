@@ -91,6 +91,23 @@ def test_kernel_choice(L):
     assert sel(128, 128, 128, A=a, B=b, C=c + 4) == sg.KERNEL_FFMA_TMA
 
 
+def test_tensor_core_modes(L):
+    a, b, c = 1 << 20, 1 << 26, 1 << 30
+    assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=True) == sg.KERNEL_TF32X3
+    assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=sg.MODE_3XTF32) == sg.KERNEL_TF32X3
+    assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=sg.MODE_TF32) == sg.KERNEL_TF32
+    # any alignment: both tensor-core paths read rounded / split copies
+    assert sel(256, 130, 127, A=a + 4, B=b + 8, C=c, tensor_cores=sg.MODE_TF32) == sg.KERNEL_TF32
+    # skinny products stay on the FP32 decode kernel in every mode
+    for mode in (sg.MODE_FP32, sg.MODE_3XTF32, sg.MODE_TF32):
+        assert sel(16, 14336, 4096, A=a, B=b, C=c, tensor_cores=mode) == sg.KERNEL_DECODE
+    assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=sg.MODE_FP32) == sg.KERNEL_FFMA_TMA
+    # an unknown mode is an argument error in the C ABI
+    assert L.sgemm_select_kernel(256, 256, 256, 1.0, a, 256, b, 256, 0.0, c, 256, 7) == sg.ERR_BAD_ARG
+    with pytest.raises(ValueError):
+        sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=5)
+
+
 def test_force_kernel(L):
     a, b, c = 1 << 20, 1 << 26, 1 << 30
     assert sg.force_kernel(99) == sg.ERR_BAD_ARG

@@ -323,6 +323,78 @@ def test_tf32x3_nan_propagates():
     assert np.isnan(C[7]).all() and np.isfinite(np.delete(C, 7, axis=0)).all()
 
 
+# ---------------------------------------------------------------- 1xTF32 (sgemm_tf32)
+# The contract: A and B rounded to TF32 (nearest, ties away), then the FP32
+# product -- checked against the oracle on rounded operands at the FP32 gate.
+TF1 = sg.KERNEL_TF32
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 8, 8), (128, 256, 16), (129, 257, 40), (300, 520, 1000),
+                                   (1000, 1000, 1000), (257, 300, 4097)])
+def test_tf32_shapes(M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "uniform", seed=M * 5 + N + K, beta=0.5)
+    _, chosen = run_checked(sg, A, B, C0, 1.25, 0.5, tensor_cores=sg.MODE_TF32)
+    assert chosen == TF1
+
+
+def test_tf32_small_integers_exact_and_layouts():
+    A, B, C0 = make_inputs(300, 200, 1000, "int", seed=6, beta=-2.0)
+    run_checked(sg, A, B, C0, 3.0, -2.0, tensor_cores=sg.MODE_TF32, exact=True)
+    A, B, C0 = make_inputs(70, 45, 33, "int", seed=13, beta=1.0)
+    for lds, offsets in [((37, 47, 46), (1, 3, 1)), ((40, 48, 48), (0, 0, 0))]:
+        run_checked(sg, A, B, C0, -1.0, 0.5, lds=lds, offsets=offsets,
+                    tensor_cores=sg.MODE_TF32, exact=True)
+
+
+def test_tf32_rounding_matches_the_oracle():
+    """With B = I the product is round(A) exactly (and round(B) with A = I), so
+    the GPU's TF32 rounding is compared with the oracle's element by element:
+    random values, values just below / at / above a tie, negative ties."""
+    import oracle
+    n = 256
+    rng = np.random.default_rng(11)
+    A = rng.standard_normal((n, n)).astype(np.float32) * 3
+    bits = A.view(np.uint32)
+    bits[:64] = (bits[:64] & 0xffffe000) | 0x1000                # exact ties
+    bits[64:96] = (bits[64:96] & 0xffffe000) | 0x0fff            # just below
+    bits[96:128] = (bits[96:128] & 0xffffe000) | 0x1001          # just above
+    eye = np.eye(n, dtype=np.float32)
+    for X, Y, want in ((A, eye, oracle.round_tf32(A)), (eye, A, oracle.round_tf32(A))):
+        dX, dY = torch.from_numpy(X).cuda(), torch.from_numpy(Y).cuda()
+        dC = torch.empty((n, n), device="cuda")
+        sg.sgemm_tf32(dX, dY, dC)
+        assert sg.status() == sg.OK
+        got = dC.cpu().numpy()
+        bad = np.flatnonzero(got.view(np.uint32) != want.view(np.uint32))
+        assert bad.size == 0, f"{bad.size} elements differ, first {got.flat[bad[0]]!r} vs {want.flat[bad[0]]!r}"
+
+
+def test_tf32_is_one_term():
+    """On uniform inputs (24 significant bits) the 1xTF32 result is within the
+    FP32 gate of the rounded-operand product but visibly off the exact one."""
+    from gpu_util import normwise_err
+    import oracle
+    M, N, K = 256, 256, 2048
+    A, B, _ = make_inputs(M, N, K, "uniform", seed=78)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.empty((M, N), device="cuda")
+    sg.sgemm_tf32(dA, dB, dC)
+    assert sg.status() == sg.OK
+    got = dC.cpu().numpy()
+    err_rounded = normwise_err(got, oracle.sgemm(A, B, inputs="tf32"), A, B, K)
+    err_exact = normwise_err(got, oracle.sgemm(A, B), A, B, K)
+    assert err_rounded <= GATE, err_rounded
+    assert err_exact > 3 * GATE, err_exact
+
+
+def test_workload_8192_tf32_sampled_rows():
+    A, B, C0, w = synth.workload_inputs("sgemm_8192")
+    C0 = np.full((w["M"], w["N"]), np.nan, np.float32)
+    _, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"], tensor_cores=sg.MODE_TF32,
+                            rows=_sample_rows(w["M"]))
+    assert chosen == TF1
+
+
 def test_workload_8192_3xtf32_sampled_rows():
     A, B, C0, w = synth.workload_inputs("sgemm_8192")
     C0 = np.full((w["M"], w["N"]), np.nan, np.float32)
