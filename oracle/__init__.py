@@ -22,6 +22,9 @@ SOURCE = os.path.join(HERE, "sgemm_oracle.c")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIBRARY = os.path.join(BUILD_DIR, "liboracle_sgemm.so")
 
+# activation ids of oracle_sgemm_rows_fused
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "silu": 3}
+
 _lock = threading.Lock()
 _default = None
 
@@ -31,7 +34,7 @@ def compile_library(source: str = SOURCE, output: str = LIBRARY, cc: str | None 
     cc = cc or os.environ.get("CC", "gcc")
     os.makedirs(os.path.dirname(output), exist_ok=True)
     tmp = output + f".tmp{os.getpid()}"
-    cmd = [cc, "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", source, "-o", tmp]
+    cmd = [cc, "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", source, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True, capture_output=True, text=True)
     os.replace(tmp, output)
     return output
@@ -83,6 +86,12 @@ class Oracle:
             _f32p, ctypes.c_int64, _f32p, ctypes.c_int64,
             ctypes.c_float, _f32p, ctypes.c_int64,
             _i64p, ctypes.c_int64, _f32p, ctypes.c_int64, ctypes.c_int]
+        self.lib.oracle_sgemm_rows_fused.restype = ctypes.c_int
+        self.lib.oracle_sgemm_rows_fused.argtypes = [
+            ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+            _f32p, ctypes.c_int64, _f32p, ctypes.c_int64,
+            ctypes.c_float, _f32p, ctypes.c_int64, _f32p, ctypes.c_int,
+            _i64p, ctypes.c_int64, _f32p, ctypes.c_int64, ctypes.c_int]
         self.lib.oracle_max_threads.restype = ctypes.c_int
         self.lib.oracle_max_threads.argtypes = []
         self.lib.oracle_round_tf32.restype = None
@@ -100,10 +109,12 @@ class Oracle:
 
     def sgemm(self, A: np.ndarray, B: np.ndarray, C0: np.ndarray | None = None,
               alpha: float = 1.0, beta: float = 0.0, rows=None,
-              threads: int = 0) -> np.ndarray:
-        """alpha*A@B + beta*C0 (rows ``rows`` only, if given) as a new float32 array.
+              threads: int = 0, bias: np.ndarray | None = None, act: str = "none") -> np.ndarray:
+        """act(alpha*A@B + beta*C0 + bias) (rows ``rows`` only, if given) as a new
+        float32 array; without ``bias`` and ``act`` the plain product.
 
-        ``A`` is M x K, ``B`` K x N, ``C0`` M x N (may be None when beta == 0).
+        ``A`` is M x K, ``B`` K x N, ``C0`` M x N (may be None when beta == 0),
+        ``bias`` N floats added to every row, ``act`` one of ACTIVATIONS.
         Row-strided views (leading dimension > row length) are passed through
         with their strides, so gap columns are never copied or read.
         """
@@ -117,10 +128,20 @@ class Oracle:
             rows = np.arange(M, dtype=np.int64)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         out = np.empty((rows.size, N), dtype=np.float32)
-        rc = self.lib.oracle_sgemm_rows(
-            M, N, K, float(alpha), _ptr(A), _ld(A), _ptr(B), _ld(B),
-            float(beta), _ptr(C0), _ld(C0),
-            rows.ctypes.data_as(_i64p), rows.size, _ptr(out), max(N, 1), int(threads))
+        if bias is None and act == "none":
+            rc = self.lib.oracle_sgemm_rows(
+                M, N, K, float(alpha), _ptr(A), _ld(A), _ptr(B), _ld(B),
+                float(beta), _ptr(C0), _ld(C0),
+                rows.ctypes.data_as(_i64p), rows.size, _ptr(out), max(N, 1), int(threads))
+        else:
+            if bias is not None:
+                bias = np.ascontiguousarray(bias, dtype=np.float32).reshape(-1)
+                if bias.size != N:
+                    raise ValueError("bias must hold N floats")
+            rc = self.lib.oracle_sgemm_rows_fused(
+                M, N, K, float(alpha), _ptr(A), _ld(A), _ptr(B), _ld(B),
+                float(beta), _ptr(C0), _ld(C0), _ptr(bias), ACTIVATIONS[act],
+                rows.ctypes.data_as(_i64p), rows.size, _ptr(out), max(N, 1), int(threads))
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
         return out
@@ -139,16 +160,19 @@ def default() -> Oracle:
     return _default
 
 
-def sgemm(A, B, C0=None, alpha=1.0, beta=0.0, rows=None, threads=0, inputs="fp32"):
-    """alpha*A@B + beta*C0 from the default oracle build (see ``Oracle.sgemm``).
+def sgemm(A, B, C0=None, alpha=1.0, beta=0.0, rows=None, threads=0, inputs="fp32",
+          bias=None, act="none"):
+    """act(alpha*A@B + beta*C0 + bias) from the default oracle build (see
+    ``Oracle.sgemm``).
 
     ``inputs="tf32"`` gives the reduced-precision product: A and B are rounded
-    to TF32 first (``round_tf32``), C0 is not."""
+    to TF32 first (``round_tf32``), C0 and bias are not."""
     if inputs == "tf32":
         A, B = round_tf32(A), round_tf32(B)
     elif inputs != "fp32":
         raise ValueError(f"unknown input precision {inputs!r}")
-    return default().sgemm(A, B, C0, alpha=alpha, beta=beta, rows=rows, threads=threads)
+    return default().sgemm(A, B, C0, alpha=alpha, beta=beta, rows=rows, threads=threads,
+                           bias=bias, act=act)
 
 
 def round_tf32(x):

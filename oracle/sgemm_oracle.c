@@ -36,6 +36,7 @@
  * the caller rounds A and B and passes the rounded copies to the functions
  * above (C0 is not rounded).
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -54,17 +55,47 @@ int oracle_max_threads(void)
 }
 
 /*
- * Rows rows[0..nrows-1] of C = alpha*A@B + beta*C0, written densely to
- * out[r*ldo + j] for r < nrows, j < N.  C0 is indexed by the true row number.
- * Returns 0, or -1 on bad arguments / allocation failure.
+ * Fused epilogue (the library's sgemm_fused): after alpha*S + beta*C0 the
+ * bias of the column is added and an activation applied, all in double,
+ * before the single rounding to float:
+ *     C[i][j] = fp32( act( alpha*S[i][j] + beta*C0[i][j] + bias[j] ) )
+ * bias == NULL adds nothing.  The activations (the pages choose none; these
+ * are the ones of the transformer FFN blocks the prefill shapes come from):
+ *   ORACLE_ACT_NONE  identity
+ *   ORACLE_ACT_RELU  x < 0 ? 0 : x                   (NaN stays NaN)
+ *   ORACLE_ACT_GELU  x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3)))
+ *                    (the tanh form of GELU)
+ *   ORACLE_ACT_SILU  x / (1 + exp(-x))
  */
-int oracle_sgemm_rows(int64_t M, int64_t N, int64_t K, float alpha,
-                      const float *A, int64_t lda, const float *B, int64_t ldb,
-                      float beta, const float *C0, int64_t ldc,
-                      const int64_t *rows, int64_t nrows,
-                      float *out, int64_t ldo, int nthreads)
+enum { ORACLE_ACT_NONE = 0, ORACLE_ACT_RELU = 1, ORACLE_ACT_GELU = 2, ORACLE_ACT_SILU = 3 };
+
+static double activate(double x, int act)
 {
-    if (M < 0 || N < 0 || K < 0 || nrows < 0 || ldo < N)
+    switch (act) {
+    case ORACLE_ACT_RELU:
+        return x < 0.0 ? 0.0 : x;
+    case ORACLE_ACT_GELU:
+        return 0.5 * x * (1.0 + tanh(0.79788456080286535588 * (x + 0.044715 * x * x * x)));
+    case ORACLE_ACT_SILU:
+        return x / (1.0 + exp(-x));
+    default:
+        return x;
+    }
+}
+
+/*
+ * Rows rows[0..nrows-1] of C = act(alpha*A@B + beta*C0 + bias), written
+ * densely to out[r*ldo + j] for r < nrows, j < N.  C0 is indexed by the true
+ * row number.  Returns 0, or -1 on bad arguments / allocation failure.
+ */
+int oracle_sgemm_rows_fused(int64_t M, int64_t N, int64_t K, float alpha,
+                            const float *A, int64_t lda, const float *B, int64_t ldb,
+                            float beta, const float *C0, int64_t ldc,
+                            const float *bias, int act,
+                            const int64_t *rows, int64_t nrows,
+                            float *out, int64_t ldo, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || nrows < 0 || ldo < N || act < 0 || act > ORACLE_ACT_SILU)
         return -1;
     const int use_ab = (alpha != 0.0f) && (K > 0);
     const int use_c = (beta != 0.0f);
@@ -111,13 +142,26 @@ int oracle_sgemm_rows(int64_t M, int64_t N, int64_t K, float alpha,
                     double v = use_ab ? (double)alpha * acc[j] : 0.0;
                     if (use_c)
                         v += (double)beta * (double)C0[i * ldc + j];
-                    orow[j] = (float)v;
+                    if (bias != NULL)
+                        v += (double)bias[j];
+                    orow[j] = (float)activate(v, act);
                 }
             }
             free(acc);
         }
     }
     return failed ? -1 : 0;
+}
+
+/* Rows of C = alpha*A@B + beta*C0 (no bias, no activation). */
+int oracle_sgemm_rows(int64_t M, int64_t N, int64_t K, float alpha,
+                      const float *A, int64_t lda, const float *B, int64_t ldb,
+                      float beta, const float *C0, int64_t ldc,
+                      const int64_t *rows, int64_t nrows,
+                      float *out, int64_t ldo, int nthreads)
+{
+    return oracle_sgemm_rows_fused(M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, NULL,
+                                   ORACLE_ACT_NONE, rows, nrows, out, ldo, nthreads);
 }
 
 /* All M rows of C = alpha*A@B + beta*C0 into out[i*ldo + j]. */

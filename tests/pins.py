@@ -254,6 +254,63 @@ def pin_tf32_nearest(orc):
     assert tie[:2000].all() and np.all(np.abs(rd[tie]) > np.abs(xd[tie])), "tie not away from zero"
 
 
+def pin_bias_relu(orc):
+    """Fused epilogue on small integers, exact in int64: the bias is per column
+    (added to every row), ReLU clamps the sum below zero, and a NaN in C0
+    reaches the output through ReLU (it is not clamped to 0)."""
+    M, N, K = 23, 17, 30
+    A = synth.matrix(M, K, seed=101, stream=0, dist="int")
+    B = synth.matrix(K, N, seed=101, stream=1, dist="int")
+    C0 = synth.matrix(M, N, seed=101, stream=2, dist="int")
+    bias = synth.matrix(1, N, seed=101, stream=3, dist="int")[0] * 8
+    exact = (A.astype(np.int64) @ B.astype(np.int64) * 2 - C0.astype(np.int64)
+             + bias.astype(np.int64)[None, :])
+    got = orc.sgemm(A, B, C0, alpha=2.0, beta=-1.0, bias=bias)
+    assert np.array_equal(got, exact.astype(np.float32))
+    got = orc.sgemm(A, B, C0, alpha=2.0, beta=-1.0, bias=bias, act="relu")
+    assert np.array_equal(got, np.maximum(exact, 0).astype(np.float32))
+    assert (exact < 0).any() and (exact > 0).any()
+    C1 = C0.copy()
+    C1[3, 4] = np.nan
+    got = orc.sgemm(A, B, C1, alpha=1.0, beta=1.0, act="relu")
+    assert np.isnan(got[3, 4]) and np.isfinite(np.delete(got.reshape(-1), 3 * N + 4)).all()
+    # alpha = 0: act(beta*C0 + bias), A and B not read
+    got = orc.sgemm(np.full((M, K), np.nan, np.float32), np.full((K, N), np.nan, np.float32), C0,
+                    alpha=0.0, beta=1.0, bias=bias, act="relu")
+    assert np.array_equal(got, np.maximum(C0.astype(np.int64) + bias[None, :], 0).astype(np.float32))
+
+
+def _act_inputs(orc):
+    """x values from -12 to 12 as the rows of A @ I (exact)."""
+    x = np.linspace(-12.0, 12.0, 481, dtype=np.float32).reshape(1, -1)
+    return x, np.eye(1, dtype=np.float32)
+
+
+def pin_gelu_silu(orc):
+    """GELU (tanh form) and SiLU on x in [-12, 12], checked against other
+    formulas, not their own: both satisfy f(x) - f(-x) = x (their "gates" g
+    obey g(x) + g(-x) = 1); GELU's tanh form stays within 1e-3 of the exact
+    erf form x*Phi(x); SiLU equals x*(1 + tanh(x/2))/2; and both tend to x for
+    large x and to 0 for large negative x."""
+    import math
+    x, eye = _act_inputs(orc)
+    xs = x.reshape(-1).astype(np.float64)
+    for act in ("gelu", "silu"):
+        f = orc.sgemm(eye, x, act=act).reshape(-1).astype(np.float64)       # f(x)
+        g = orc.sgemm(eye, -x, act=act).reshape(-1).astype(np.float64)      # f(-x)
+        tol = 4 * 2.0 ** -24 * np.maximum(np.abs(f), np.abs(g)) + 1e-30
+        assert np.all(np.abs((f - g) - xs) <= tol + 2.0 ** -24 * np.abs(xs)), act
+        assert abs(f[-1] - 12.0) < 1e-4 and abs(f[0]) < 1e-4, act   # 12*sigmoid(-12) = 7.4e-5
+    gelu = orc.sgemm(eye, x, act="gelu").reshape(-1).astype(np.float64)
+    exact = np.array([v * 0.5 * (1.0 + math.erf(v / math.sqrt(2.0))) for v in xs])
+    assert np.max(np.abs(gelu - exact)) < 1e-3
+    assert np.max(np.abs(gelu - exact)) > 1e-5     # the tanh form, not the erf form
+    silu = orc.sgemm(eye, x, act="silu").reshape(-1).astype(np.float64)
+    other = xs * (1.0 + np.tanh(xs / 2.0)) / 2.0
+    assert np.all(np.abs(silu - other) <= 2.0 ** -22 * np.abs(other) + 1e-30)
+
+
 ALL_PINS = [pin_small_int_exact, pin_exact_rational, pin_identity, pin_permutation,
             pin_rank1, pin_transpose, pin_freivalds, pin_alpha_beta, pin_ld_gaps,
-            pin_row_subset, pin_tf32_exact_cases, pin_tf32_nearest]
+            pin_row_subset, pin_tf32_exact_cases, pin_tf32_nearest, pin_bias_relu,
+            pin_gelu_silu]

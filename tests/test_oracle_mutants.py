@@ -44,6 +44,12 @@ MUTANTS = [
     ("tf32_ties_even", "u = (u + 0x1000u) & 0xffffe000u;",
      "u = (u + 0x0fffu + ((u >> 13) & 1u)) & 0xffffe000u;"),
     ("tf32_keeps_11_bits", "u = (u + 0x1000u) & 0xffffe000u;", "u = (u + 0x0800u) & 0xfffff000u;"),
+    ("bias_by_row", "v += (double)bias[j];", "v += (double)bias[i % N];"),
+    ("act_before_bias", "orow[j] = (float)activate(v, act);",
+     "orow[j] = (float)(activate(v - (bias ? (double)bias[j] : 0.0), act) + (bias ? (double)bias[j] : 0.0));"),
+    ("gelu_coefficient", "(x + 0.044715 * x * x * x)", "(x + 0.04715 * x * x * x)"),
+    ("silu_sign", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
+    ("relu_nan_to_zero", "return x < 0.0 ? 0.0 : x;", "return x > 0.0 ? x : 0.0;"),
 ]
 
 CHILD = textwrap.dedent("""
