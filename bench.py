@@ -260,14 +260,16 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3):
     g = torch.Generator(device=dev)
     g.manual_seed(3)
 
-    def bench_shape(M, N, K, sigma_b, tensor_cores=False):
+    def bench_shape(M, N, K, sigma_b, tensor_cores=False, activation="none"):
         """Mean ms per call of `steps` calls captured in one CUDA graph and
         replayed (the launch gaps of eager calls excluded), after warm-up calls
         that also size the workspace so that capture allocates nothing."""
         A = torch.randn((M, K), device=dev, generator=g)
         B = torch.randn((K, N), device=dev, generator=g) * sigma_b
         C = torch.empty((M, N), device=dev)
-        fn = lambda: sg.sgemm(A, B, C, 1.0, 0.0, stream=stream, tensor_cores=tensor_cores)
+        bias = torch.randn((N,), device=dev, generator=g) if activation != "none" else None
+        fn = lambda: sg.sgemm(A, B, C, 1.0, 0.0, stream=stream, tensor_cores=tensor_cores,
+                              bias=bias, activation=activation)
         for _ in range(warmup):
             fn()
         torch.cuda.synchronize()
@@ -288,7 +290,7 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3):
         st = sg.status(stream)
         kid = sg.select_kernel(M, N, K, 1.0, A.data_ptr(), K, B.data_ptr(), N, 0.0,
                                C.data_ptr(), N, tensor_cores)
-        del A, B, C, graph
+        del A, B, C, bias, graph
         return per, st, sg.KERNEL_NAMES.get(kid, str(kid)), per_eager
 
     for M in (1, 4, 16):
@@ -306,6 +308,11 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3):
         per, st, kn, pe = bench_shape(M, N, K, sb)
         out[name] = {"shape": [M, N, K], "kernel": kn, "ms": per, "status": st,
                      "TFLOP/s": 2 * M * N * K / (per * 1e-3) / 1e12, "ms_eager": pe}
+    # the FFN-up GEMM with the fused epilogue act(X W + bias), SiLU
+    per, st, kn, pe = bench_shape(8192, 14336, 4096, 0.02, activation="silu")
+    out["prefill_up_bias_silu"] = {"shape": [8192, 14336, 4096], "kernel": kn, "ms": per,
+                                   "status": st, "TFLOP/s": 2 * 8192 * 14336 * 4096 / (per * 1e-3) / 1e12,
+                                   "ms_eager": pe, "epilogue": "bias + SiLU (sgemm_fused)"}
     # Medium and skinny shapes whose last wave is split along K.  Their
     # operands (4-34 MB) stay in L2 between repetitions: timing only.
     mid = [("mid_1024", 1024, 1024, 1024), ("mid_1024x1024x8192", 1024, 1024, 8192),

@@ -29,6 +29,8 @@ KERNEL_FFMA_GENERIC, KERNEL_DECODE, KERNEL_TF32X3, KERNEL_TF32 = 4, 5, 6, 7
 KERNEL_NAMES = {KERNEL_NONE: "none", KERNEL_SCALE_C: "scale_c", KERNEL_FFMA_TMA: "ffma_tma",
                 KERNEL_FFMA_GENERIC: "ffma_generic", KERNEL_DECODE: "decode",
                 KERNEL_TF32X3: "tf32x3", KERNEL_TF32: "tf32"}
+# activations of the fused epilogue (sgemm_fused)
+ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "silu": 3}
 # arithmetic of a call (sgemm, sgemm_3xtf32, sgemm_tf32)
 MODE_FP32, MODE_3XTF32, MODE_TF32 = 0, 1, 2
 _ENTRY = {MODE_FP32: "sgemm", MODE_3XTF32: "sgemm_3xtf32", MODE_TF32: "sgemm_tf32"}
@@ -69,6 +71,8 @@ def lib() -> ctypes.CDLL:
         for name in ("sgemm", "sgemm_3xtf32", "sgemm_tf32"):
             getattr(L, name).argtypes = _GEMM_ARGS
             getattr(L, name).restype = ctypes.c_int
+        L.sgemm_fused.argtypes = _GEMM_ARGS[:-1] + [_vp, ctypes.c_int, ctypes.c_int, _vp]
+        L.sgemm_fused.restype = ctypes.c_int
         L.sgemm_select_kernel.argtypes = _GEMM_ARGS[:-1] + [ctypes.c_int]
         L.sgemm_select_kernel.restype = ctypes.c_int
         L.sgemm_status.argtypes = [_vp]
@@ -136,15 +140,17 @@ def sgemm_ptr(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=0, tensor_cor
 
 
 def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
-          tensor_cores: bool = False) -> None:
+          tensor_cores: bool = False, bias=None, activation: str = "none") -> None:
     """C <- alpha * A @ B + beta * C in place on torch CUDA float32 tensors.
 
     A is (M, K), B (K, N), C (M, N); each may be a row-strided view (row
     stride >= row length).  Enqueued on ``stream`` (default: the current torch
     stream of C's device); returns without waiting.  ``tensor_cores`` selects
     the arithmetic: False (FP32 FFMA), True (3xTF32 tcgen05 path) or a MODE_*
-    value (MODE_TF32: the reduced-precision 1xTF32 path).  Raises SgemmError
-    on a rejected call.
+    value (MODE_TF32: the reduced-precision 1xTF32 path).  ``bias`` (a CUDA
+    float32 tensor of N elements) and ``activation`` (a key of ACTIVATIONS)
+    select the fused epilogue C = act(alpha*A@B + beta*C + bias) of
+    sgemm_fused.  Raises SgemmError on a rejected call.
     """
     for t, n in ((A, "A"), (B, "B"), (C, "C")):
         _check_operand(t, n)
@@ -153,11 +159,27 @@ def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
     if K2 != K or tuple(C.shape) != (M, N):
         raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
     dev = C.device if C.is_cuda else None
-    rc = sgemm_ptr(M, N, K, float(alpha), A.data_ptr() or None, _ld(A), B.data_ptr() or None,
-                   _ld(B), float(beta), C.data_ptr() or None, _ld(C),
-                   _stream_handle(stream, dev), tensor_cores)
+    if bias is None and activation == "none":
+        rc = sgemm_ptr(M, N, K, float(alpha), A.data_ptr() or None, _ld(A), B.data_ptr() or None,
+                       _ld(B), float(beta), C.data_ptr() or None, _ld(C),
+                       _stream_handle(stream, dev), tensor_cores)
+        if rc != OK:
+            raise SgemmError(rc, _ENTRY[_mode(tensor_cores)])
+        return
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}; one of {sorted(ACTIVATIONS)}")
+    if bias is not None:
+        import torch
+        if (not isinstance(bias, torch.Tensor) or bias.dtype != torch.float32 or bias.numel() != N
+                or (N and (not bias.is_cuda or not bias.is_contiguous()))):
+            raise TypeError("bias must be a contiguous CUDA float32 tensor of N elements")
+    rc = int(lib().sgemm_fused(M, N, K, float(alpha), A.data_ptr() or None, _ld(A),
+                               B.data_ptr() or None, _ld(B), float(beta), C.data_ptr() or None,
+                               _ld(C), bias.data_ptr() if bias is not None and N else None,
+                               ACTIVATIONS[activation], _mode(tensor_cores),
+                               _stream_handle(stream, dev)))
     if rc != OK:
-        raise SgemmError(rc, _ENTRY[_mode(tensor_cores)])
+        raise SgemmError(rc, "sgemm_fused")
 
 
 def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:

@@ -201,10 +201,24 @@ int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t
     return SGEMM_ERR_BAD_DIM;
 }
 
+// The fused epilogue's own arguments: a known activation, and a bias (N
+// floats) that does not overlap C.
+int check_epilogue(int64_t M, int64_t N, const float *C, int64_t ldc, const float *bias, int act) {
+    if (act < SGEMM_ACT_NONE || act > SGEMM_ACT_SILU) return SGEMM_ERR_BAD_ARG;
+    if (bias == nullptr || M == 0 || N == 0) return SGEMM_OK;
+    uintptr_t c0, c1, v0, v1;
+    span(C, M, N, ldc, &c0, &c1);
+    span(bias, 1, N, N, &v0, &v1);
+    return overlaps(c0, c1, v0, v1) ? SGEMM_ERR_ALIAS : SGEMM_OK;
+}
+
 int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda, const float *B,
-        int64_t ldb, float beta, float *C, int64_t ldc, void *stream, int mode) {
+        int64_t ldb, float beta, float *C, int64_t ldc, void *stream, int mode,
+        const float *bias = nullptr, int act = SGEMM_ACT_NONE) {
     const int kid = choose(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode);
     if (kid < 0) return kid;
+    const int erc = check_epilogue(M, N, C, ldc, bias, act);
+    if (erc != SGEMM_OK) return erc;
     if (kid == SGEMM_KERNEL_NONE) return SGEMM_OK;
     DeviceState *st = nullptr;
     const int ds = device_state(&st);
@@ -219,6 +233,8 @@ int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t ld
     g.wait_ns = (uint64_t)g_wait_ns.load();
     g.sm_count = st->sm_count;
     g.encode = g_encode;
+    g.bias = bias;
+    g.act = act;
 
     cudaError_t e = cudaSuccess;
     switch (kid) {
@@ -313,6 +329,12 @@ int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, i
 int sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
                const float *B, int64_t ldb, float beta, float *C, int64_t ldc, void *stream) {
     return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, SGEMM_MODE_TF32);
+}
+
+int sgemm_fused(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+                const float *B, int64_t ldb, float beta, float *C, int64_t ldc, const float *bias,
+                int activation, int mode, void *stream) {
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, mode, bias, activation);
 }
 
 int sgemm_status(void *stream) {

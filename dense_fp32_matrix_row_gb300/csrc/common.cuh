@@ -19,6 +19,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 // Everything a kernel launcher needs.
+// Activations of the fused epilogue (the SGEMM_ACT_* values of the C ABI).
+enum : int { kActNone = 0, kActRelu = 1, kActGelu = 2, kActSilu = 3 };
+
+// What every kernel's store applies to an accumulated dot product `acc`:
+//     C = act(alpha*acc + beta*C + bias[col])
+// C is read only when beta != 0; bias == nullptr adds nothing.
+struct Epilogue {
+    float alpha, beta;
+    const float *bias;
+    int act;
+};
+
 struct GemmArgs {
     int64_t M, N, K;
     float alpha, beta;
@@ -30,6 +42,9 @@ struct GemmArgs {
     uint64_t wait_ns;       // bounded-wait limit in nanoseconds
     int sm_count;
     EncodeTiledFn encode;   // tensor-map encoder
+    const float *bias = nullptr;   // fused epilogue: N floats, or none
+    int act = kActNone;            // fused epilogue activation
+    Epilogue epi() const { return Epilogue{alpha, beta, bias, act}; }
 };
 
 // 2-D fp32 tensor map over a row-major matrix: `inner` contiguous elements
@@ -81,6 +96,20 @@ int fill_device_args(GemmArgs &g);
 
 
 #ifdef __CUDACC__
+
+// act(v + bias[col]): the part of the epilogue after alpha*acc + beta*C.
+// GELU is the tanh form x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))),
+// SiLU is x / (1 + e^-x); CUDA's tanhf and expf.  ReLU keeps NaN.
+__device__ __forceinline__ float epilogue_tail(const Epilogue &e, float v, int64_t col) {
+    if (e.bias != nullptr) v += __ldg(e.bias + col);
+    switch (e.act) {
+        case kActRelu: return v < 0.0f ? 0.0f : v;
+        case kActGelu:
+            return 0.5f * v * (1.0f + tanhf(0.7978845608028654f * fmaf(0.044715f * v, v * v, v)));
+        case kActSilu: return v / (1.0f + expf(-v));
+        default: return v;
+    }
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -18,7 +18,8 @@
 //    cluster through distributed shared memory; both sums run in a fixed
 //    order, so results do not depend on timing;
 //  * block `rank` finishes outputs [rank*per, (rank+1)*per) of the 128*MT the
-//    cluster owns and applies C = alpha*sum + beta*C (C read only if beta != 0).
+//    cluster owns and applies C = act(alpha*sum + beta*C + bias) (C read only
+//    if beta != 0).
 #include <cooperative_groups.h>
 
 #include <atomic>
@@ -89,8 +90,8 @@ __device__ __forceinline__ void fma_row(float (&acc)[MT][4], const float *__rest
 
 template <int MT, bool VEC>
 __global__ void __launch_bounds__(DTHREADS)
-decode_kernel(int M, int64_t N, int64_t K, float alpha, const float *__restrict__ A, int64_t lda,
-              const float *__restrict__ B, int64_t ldb, float beta, float *__restrict__ C,
+decode_kernel(int M, int64_t N, int64_t K, Epilogue ep, const float *__restrict__ A, int64_t lda,
+              const float *__restrict__ B, int64_t ldb, float *__restrict__ C,
               int64_t ldc, int64_t kslice) {
     extern __shared__ float4 smem4[];
     float *smem = reinterpret_cast<float *>(smem4);
@@ -166,8 +167,8 @@ decode_kernel(int M, int64_t N, int64_t K, float alpha, const float *__restrict_
         const int64_t gn = n0 + (o - m * DCOLS);
         if (m < M && gn < N) {
             float *p = C + (int64_t)m * ldc + gn;
-            const float v = alpha * s;
-            *p = (beta != 0.0f) ? fmaf(beta, *p, v) : v;
+            const float v = ep.alpha * s;
+            *p = epilogue_tail(ep, (ep.beta != 0.0f) ? fmaf(ep.beta, *p, v) : v, gn);
         }
     }
     cluster.sync();   // keep this block's `part` alive until every peer has read it
@@ -198,8 +199,8 @@ cudaError_t launch_mt(const GemmArgs &g) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha, g.A,
-                              g.lda, g.B, g.ldb, g.beta, g.C, g.ldc, kslice);
+    return cudaLaunchKernelEx(&cfg, kern, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.epi(), g.A,
+                              g.lda, g.B, g.ldb, g.C, g.ldc, kslice);
 }
 
 // ---------------------------------------------------------------- TMA-streamed variant
@@ -243,7 +244,7 @@ struct TmaCfg {
 template <class T, int MT, int TNV, int DW, int TSTAGES>
 __global__ void __launch_bounds__(DW * 32, DECODE_MINB)
 decode_tma_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int64_t K,
-                  float alpha, const float *__restrict__ A, int64_t lda, float beta,
+                  Epilogue ep, const float *__restrict__ A, int64_t lda,
                   float *__restrict__ C, int64_t ldc, int64_t kslice, unsigned *err,
                   uint64_t wait_ns) {
     using L = T;
@@ -386,8 +387,8 @@ decode_tma_kernel(const __grid_constant__ CUtensorMap tmB, int M, int64_t N, int
         const int64_t gn = n0 + (o - m * COLS);
         if (!any_failed && m < M && gn < N) {
             float *p = C + (int64_t)m * ldc + gn;
-            const float v = alpha * sum;
-            *p = (beta != 0.0f) ? fmaf(beta, *p, v) : v;
+            const float v = ep.alpha * sum;
+            *p = epilogue_tail(ep, (ep.beta != 0.0f) ? fmaf(ep.beta, *p, v) : v, gn);
         }
     }
     cluster.sync();
@@ -474,7 +475,7 @@ struct DoCfg {
 template <int MT, int RG>
 __global__ void __launch_bounds__(DO_THREADS, DoCfg<MT, RG>::MINB)
 decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmA,
-                    int M, int64_t N, int64_t K, float alpha, float beta, float *__restrict__ C,
+                    int M, int64_t N, int64_t K, Epilogue ep, float *__restrict__ C,
                     int64_t ldc, int64_t kslice, unsigned *err, uint64_t wait_ns) {
     using L = DoCfg<MT, RG>;
     constexpr int KG = L::KG, MTL = L::MTL;
@@ -625,8 +626,8 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (gn + e < N) {
-                    const float v = alpha * sv[e];
-                    p[e] = (beta != 0.0f) ? fmaf(beta, p[e], v) : v;
+                    const float v = ep.alpha * sv[e];
+                    p[e] = epilogue_tail(ep, (ep.beta != 0.0f) ? fmaf(ep.beta, p[e], v) : v, gn + e);
                 }
             }
         }
@@ -682,8 +683,8 @@ cudaError_t launch_tma(const GemmArgs &g) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmB, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha, g.A,
-                              g.lda, g.beta, g.C, g.ldc, kslice, g.err, g.wait_ns);
+    return cudaLaunchKernelEx(&cfg, kern, tmB, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.epi(), g.A,
+                              g.lda, g.C, g.ldc, kslice, g.err, g.wait_ns);
 }
 
 #ifndef DECODE_TNV
@@ -787,8 +788,8 @@ cudaError_t launch_outer(const GemmArgs &g) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tmB, tmA, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.alpha,
-                              g.beta, g.C, g.ldc, kslice, g.err, g.wait_ns);
+    return cudaLaunchKernelEx(&cfg, kern, tmB, tmA, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.epi(),
+                              g.C, g.ldc, kslice, g.err, g.wait_ns);
 }
 
 template <int MT>

@@ -1,6 +1,6 @@
 // ffma_generic.cu -- the SGEMM kernel for operands the TMA path cannot take
 // (pointers not 16-byte aligned, or a leading dimension not a multiple of 4),
-// plus the C <- beta*C kernel used when K == 0 or alpha == 0.
+// plus the C <- act(beta*C + bias) kernel used when K == 0 or alpha == 0.
 //
 // Method: shared-memory cache blocking with a per-thread register tile, as in
 // "CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", sections "3. Kernel 3"
@@ -17,8 +17,8 @@ namespace {
 constexpr int GBM = 64, GBN = 64, GBK = 16, GTM = 4, GTN = 4, GTHREADS = 256;
 
 __global__ void __launch_bounds__(GTHREADS)
-ffma_generic_kernel(int64_t M, int64_t N, int64_t K, float alpha, const float *__restrict__ A,
-                    int64_t lda, const float *__restrict__ B, int64_t ldb, float beta,
+ffma_generic_kernel(int64_t M, int64_t N, int64_t K, Epilogue ep, const float *__restrict__ A,
+                    int64_t lda, const float *__restrict__ B, int64_t ldb,
                     float *__restrict__ C, int64_t ldc) {
     // A is stored k-major (transposed) so that both operands are read as
     // float4 along the output dimension; +4 keeps rows 16-byte aligned.
@@ -76,20 +76,20 @@ ffma_generic_kernel(int64_t M, int64_t N, int64_t K, float alpha, const float *_
             const int64_t gn = n0 + tx * GTN + j;
             if (gn >= N) continue;
             float *p = C + gm * ldc + gn;
-            const float v = alpha * acc[i][j];
-            *p = (beta != 0.0f) ? fmaf(beta, *p, v) : v;
+            const float v = ep.alpha * acc[i][j];
+            *p = epilogue_tail(ep, (ep.beta != 0.0f) ? fmaf(ep.beta, *p, v) : v, gn);
         }
     }
 }
 
-// C <- beta * C; beta == 0 writes zeros without reading C.
+// C <- act(beta * C + bias); beta == 0 does not read C.
 __global__ void __launch_bounds__(256)
-scale_c_kernel(int64_t M, int64_t N, float beta, float *__restrict__ C, int64_t ldc) {
+scale_c_kernel(int64_t M, int64_t N, Epilogue ep, float *__restrict__ C, int64_t ldc) {
     for (int64_t i = blockIdx.y; i < M; i += gridDim.y) {
         float *row = C + i * ldc;
         for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < N;
              j += (int64_t)gridDim.x * blockDim.x)
-            row[j] = (beta != 0.0f) ? beta * row[j] : 0.0f;
+            row[j] = epilogue_tail(ep, (ep.beta != 0.0f) ? ep.beta * row[j] : 0.0f, j);
     }
 }
 
@@ -98,15 +98,15 @@ scale_c_kernel(int64_t M, int64_t N, float beta, float *__restrict__ C, int64_t 
 cudaError_t launch_ffma_generic(const GemmArgs &g) {
     const dim3 grid((unsigned)((g.N + GBN - 1) / GBN), (unsigned)((g.M + GBM - 1) / GBM));
     if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-    ffma_generic_kernel<<<grid, GTHREADS, 0, g.stream>>>(g.M, g.N, g.K, g.alpha, g.A, g.lda, g.B,
-                                                         g.ldb, g.beta, g.C, g.ldc);
+    ffma_generic_kernel<<<grid, GTHREADS, 0, g.stream>>>(g.M, g.N, g.K, g.epi(), g.A, g.lda, g.B,
+                                                         g.ldb, g.C, g.ldc);
     return cudaGetLastError();
 }
 
 cudaError_t launch_scale_c(const GemmArgs &g) {
     const int64_t gx = (g.N + 255) / 256;
     const dim3 grid((unsigned)(gx < 64 ? gx : 64), (unsigned)(g.M < 65535 ? g.M : 65535));
-    scale_c_kernel<<<grid, 256, 0, g.stream>>>(g.M, g.N, g.beta, g.C, g.ldc);
+    scale_c_kernel<<<grid, 256, 0, g.stream>>>(g.M, g.N, g.epi(), g.C, g.ldc);
     return cudaGetLastError();
 }
 

@@ -27,7 +27,7 @@
 //    拆解（一）", section "共享内存的内部结构：32 个 bank");
 //  * K tails and M/N edge tiles are zero-filled by TMA (out-of-range box
 //    elements read as 0) and the epilogue guards its stores; the epilogue
-//    applies C = alpha*acc + beta*C, reading C only when beta != 0.
+//    applies C = act(alpha*acc + beta*C + bias), reading C only when beta != 0.
 //
 // Lane (ty, tx) of warp (wm, wn) owns rows    wm*4*TM + 16*(i/4) + 4*ty + i%4   (i < TM)
 //                                 and columns wn*8*TN + 32*(j/4) + 4*tx + j%4   (j < TN).
@@ -126,14 +126,14 @@ __device__ __forceinline__ void compute_stage(float (&acc)[C::TM][C::TN], const 
     }
 }
 
-// C = alpha*acc + beta*C for this lane's outputs of the tile at (m0, n0);
-// C is read only when beta != 0, stores are guarded at the matrix edge.
+// C = act(alpha*acc + beta*C + bias) for this lane's outputs of the tile at
+// (m0, n0); C is read only when beta != 0, stores are guarded at the matrix edge.
 template <class C>
 __device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int m0, int n0,
-                                           int arow, int bcol, int M, int N, float alpha,
-                                           float beta, float *__restrict__ Cm, int64_t ldc,
-                                           int c_vec4) {
+                                           int arow, int bcol, int M, int N, const Epilogue &ep,
+                                           float *__restrict__ Cm, int64_t ldc, int c_vec4) {
     constexpr int TM = C::TM, TN = C::TN;
+    const bool tail = ep.bias != nullptr || ep.act != kActNone;
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
         const int gm = m0 + arow + 16 * (i / 4) + (i % 4);
@@ -144,15 +144,19 @@ __device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int
             const int gn = n0 + bcol + 32 * h;
             float v[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[e] = alpha * acc[i][4 * h + e];
+            for (int e = 0; e < 4; ++e) v[e] = ep.alpha * acc[i][4 * h + e];
             if (c_vec4 && gn + 3 < N) {
                 float4 *p = reinterpret_cast<float4 *>(crow + gn);
-                if (beta != 0.0f) {
+                if (ep.beta != 0.0f) {
                     const float4 o = *p;
-                    v[0] = fmaf(beta, o.x, v[0]);
-                    v[1] = fmaf(beta, o.y, v[1]);
-                    v[2] = fmaf(beta, o.z, v[2]);
-                    v[3] = fmaf(beta, o.w, v[3]);
+                    v[0] = fmaf(ep.beta, o.x, v[0]);
+                    v[1] = fmaf(ep.beta, o.y, v[1]);
+                    v[2] = fmaf(ep.beta, o.z, v[2]);
+                    v[3] = fmaf(ep.beta, o.w, v[3]);
+                }
+                if (tail) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[e] = epilogue_tail(ep, v[e], gn + e);
                 }
                 *p = make_float4(v[0], v[1], v[2], v[3]);
             } else {
@@ -160,7 +164,9 @@ __device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int
                 for (int e = 0; e < 4; ++e) {
                     if (gn + e < N) {
                         float *p = crow + gn + e;
-                        *p = (beta != 0.0f) ? fmaf(beta, *p, v[e]) : v[e];
+                        float w = (ep.beta != 0.0f) ? fmaf(ep.beta, *p, v[e]) : v[e];
+                        if (tail) w = epilogue_tail(ep, w, gn + e);
+                        *p = w;
                     }
                 }
             }
@@ -188,7 +194,7 @@ struct TailSplit {
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmB,
-                int M, int N, int K, float alpha, float beta, float *__restrict__ Cm, int64_t ldc,
+                int M, int N, int K, Epilogue ep, float *__restrict__ Cm, int64_t ldc,
                 int c_vec4, TailSplit ts, unsigned *err, uint64_t wait_ns) {
     constexpr int TM = C::TM, TN = C::TN, BK = C::BK, BM = C::BM, BN = C::BN, STAGES = C::STAGES;
     extern __shared__ unsigned char smem_raw[];
@@ -287,7 +293,7 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
 
     // ---------------------------------------------------------------- epilogue
     if (part < 0) {
-        if (!any_failed) store_tile<C>(acc, m0, n0, arow, bcol, M, N, alpha, beta, Cm, ldc, c_vec4);
+        if (!any_failed) store_tile<C>(acc, m0, n0, arow, bcol, M, N, ep, Cm, ldc, c_vec4);
         return;
     }
     // Partial tile, thread-interleaved so that each warp writes whole lines.
@@ -325,7 +331,7 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
                 }
             }
     }
-    store_tile<C>(acc, m0, n0, arow, bcol, M, N, alpha, beta, Cm, ldc, c_vec4);
+    store_tile<C>(acc, m0, n0, arow, bcol, M, N, ep, Cm, ldc, c_vec4);
 }
 
 // CTAs of the kernel one SM holds, per device (0 until asked).
@@ -409,7 +415,7 @@ cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt, const Pl
     ts.partials = extra != nullptr ? extra + kCounterFloats : nullptr;
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
     ffma_tma_kernel<C><<<(unsigned)p.units(), C::THREADS, C::SMEM, g.stream>>>(
-        tmAt, tmB, (int)g.M, (int)g.N, (int)g.K, g.alpha, g.beta, g.C, g.ldc, c_vec4, ts, g.err,
+        tmAt, tmB, (int)g.M, (int)g.N, (int)g.K, g.epi(), g.C, g.ldc, c_vec4, ts, g.err,
         g.wait_ns);
     return cudaGetLastError();
 }

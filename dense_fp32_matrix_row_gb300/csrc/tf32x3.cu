@@ -127,7 +127,7 @@ template <int TERMS>
 __global__ void __launch_bounds__(THREADS, 1)
 tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
                 const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
-                int M, int N, int K, float alpha, float beta, float *__restrict__ C, int64_t ldc,
+                int M, int N, int K, Epilogue ep, float *__restrict__ C, int64_t ldc,
                 int c_vec4, unsigned *err, uint64_t wait_ns) {
     using L = TfCfg<TERMS>;
     constexpr int TSTG = L::TSTG;
@@ -303,6 +303,7 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
             if (lane == 0) record_error(err, kErrWaitTimeout);
         } else {
             const int gm = m0 + lane_base + lane;
+            const bool tail = ep.bias != nullptr || ep.act != kActNone;
             if (gm < M) {
                 float *crow = C + (int64_t)gm * ldc;
 #pragma unroll
@@ -310,15 +311,19 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                     const int gn = n0 + col_base + 4 * q;
                     float o[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e] = alpha * acc[4 * q + e];
+                    for (int e = 0; e < 4; ++e) o[e] = ep.alpha * acc[4 * q + e];
                     if (c_vec4 && gn + 3 < N) {
                         float4 *p = reinterpret_cast<float4 *>(crow + gn);
-                        if (beta != 0.0f) {
+                        if (ep.beta != 0.0f) {
                             const float4 cv = *p;
-                            o[0] = fmaf(beta, cv.x, o[0]);
-                            o[1] = fmaf(beta, cv.y, o[1]);
-                            o[2] = fmaf(beta, cv.z, o[2]);
-                            o[3] = fmaf(beta, cv.w, o[3]);
+                            o[0] = fmaf(ep.beta, cv.x, o[0]);
+                            o[1] = fmaf(ep.beta, cv.y, o[1]);
+                            o[2] = fmaf(ep.beta, cv.z, o[2]);
+                            o[3] = fmaf(ep.beta, cv.w, o[3]);
+                        }
+                        if (tail) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) o[e] = epilogue_tail(ep, o[e], gn + e);
                         }
                         *p = make_float4(o[0], o[1], o[2], o[3]);
                     } else {
@@ -326,7 +331,8 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                         for (int e = 0; e < 4; ++e) {
                             if (gn + e < N) {
                                 float *p = crow + gn + e;
-                                *p = (beta != 0.0f) ? fmaf(beta, *p, o[e]) : o[e];
+                                const float w = (ep.beta != 0.0f) ? fmaf(ep.beta, *p, o[e]) : o[e];
+                                *p = tail ? epilogue_tail(ep, w, gn + e) : w;
                             }
                         }
                     }
@@ -386,7 +392,7 @@ cudaError_t launch_terms(const GemmArgs &g, float *ws) {
     const dim3 grid((unsigned)tiles);
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
     tf32_mma_kernel<TERMS><<<grid, THREADS, L::SMEM, g.stream>>>(
-        tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N, (int)g.K, g.alpha, g.beta, g.C, g.ldc, c_vec4,
+        tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N, (int)g.K, g.epi(), g.C, g.ldc, c_vec4,
         g.err, g.wait_ns);
     return cudaGetLastError();
 }

@@ -80,7 +80,13 @@ extern "C" {
 #define SGEMM_KERNEL_TF32X3        6   /* 3xTF32 tensor-core kernel (sgemm_3xtf32) */
 #define SGEMM_KERNEL_TF32          7   /* 1xTF32 tensor-core kernel (sgemm_tf32) */
 
-/* Arithmetic of a call, for sgemm_select_kernel's `mode`. */
+/* Activations of sgemm_fused's epilogue. */
+#define SGEMM_ACT_NONE   0   /* identity */
+#define SGEMM_ACT_RELU   1   /* x < 0 ? 0 : x (NaN stays NaN) */
+#define SGEMM_ACT_GELU   2   /* x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))) */
+#define SGEMM_ACT_SILU   3   /* x / (1 + exp(-x)) */
+
+/* Arithmetic of a call, for sgemm_select_kernel's and sgemm_fused's `mode`. */
 #define SGEMM_MODE_FP32    0   /* sgemm() */
 #define SGEMM_MODE_3XTF32  1   /* sgemm_3xtf32() */
 #define SGEMM_MODE_TF32    2   /* sgemm_tf32() */
@@ -156,6 +162,32 @@ int sgemm_3xtf32(int64_t M, int64_t N, int64_t K, float alpha,
 int sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha,
                const float *A, int64_t lda, const float *B, int64_t ldb,
                float beta, float *C, int64_t ldc, void *stream);
+
+/*
+ * sgemm_fused -- sgemm() with the epilogue extended by a bias and an
+ * activation, applied to each output before it is stored:
+ *
+ *     C = act(alpha * A @ B + beta * C + bias[j])      (j: the column)
+ *
+ * The pages fuse elementwise work into the producing kernel ("GPU 基础原理",
+ * section "4.1 算子融合", with relu(x + 1) as the example) and feed GEMMs into
+ * the transformer FFN
+ * ("GPU GEMM 优化完全拆解（一）", section "LLM 推理本质上是 GEMM 的串联") but choose
+ * no activation; these are the ones of such FFN blocks.
+ *   bias        device pointer to N floats (one per column), or NULL for none;
+ *               must not overlap C (SGEMM_ERR_ALIAS)
+ *   activation  SGEMM_ACT_*; anything else is SGEMM_ERR_BAD_ARG
+ *   mode        SGEMM_MODE_*: the arithmetic of sgemm(), sgemm_3xtf32() or
+ *               sgemm_tf32(), with the same kernels and accuracy contracts
+ * alpha*acc + beta*C + bias is formed in FP32 and the activation applied in
+ * FP32 with CUDA's tanhf / expf.  When K == 0 or alpha == 0 the result is
+ * act(beta * C + bias), A and B unread.  Other arguments, conventions and
+ * errors are those of sgemm().
+ */
+int sgemm_fused(int64_t M, int64_t N, int64_t K, float alpha,
+                const float *A, int64_t lda, const float *B, int64_t ldb,
+                float beta, float *C, int64_t ldc, const float *bias, int activation,
+                int mode, void *stream);
 
 /*
  * sgemm_status -- wait for `stream`, then report and clear the current

@@ -12,13 +12,15 @@ CANARY_BITS = np.uint32(0x7FC0DEAD)   # a quiet NaN with a recognisable payload
 GATE = 1e-6
 
 
-def normwise_err(C, Cref, A, B, K, alpha=1.0, beta=0.0, C0=None):
-    """max|C - C_ref| / (|alpha|*K*max|A|*max|B| + |beta|*max|C0|).
+def normwise_err(C, Cref, A, B, K, alpha=1.0, beta=0.0, C0=None, bias=None):
+    """max|C - C_ref| / (|alpha|*K*max|A|*max|B| + |beta|*max|C0| + max|bias|).
 
-    The denominator bounds the magnitude of every term of alpha*A@B + beta*C0.
-    With alpha = 1 and beta = 0 it is the acceptance gate's K*max|A|*max|B|;
-    the beta*C0 term is added because an output dominated by beta*C0 carries
-    a rounding error proportional to |beta*C0| that no FP32 result can avoid.
+    The denominator bounds the magnitude of every term of alpha*A@B + beta*C0
+    + bias.  With alpha = 1, beta = 0 and no bias it is the acceptance gate's
+    K*max|A|*max|B|; the beta*C0 and bias terms are added because an output
+    dominated by them carries a rounding error proportional to their size that
+    no FP32 result can avoid.  The fused activations (ReLU, GELU, SiLU) have
+    slopes below 1.13, so they leave this bound's scale unchanged.
     """
     diff = np.abs(C.astype(np.float64) - Cref.astype(np.float64))
     if diff.size == 0:
@@ -28,7 +30,8 @@ def normwise_err(C, Cref, A, B, K, alpha=1.0, beta=0.0, C0=None):
     amax = float(np.abs(A).max()) if A.size else 0.0
     bmax = float(np.abs(B).max()) if B.size else 0.0
     cmax = float(np.abs(C0).max()) if (beta != 0.0 and C0 is not None and C0.size) else 0.0
-    scale = abs(alpha) * K * amax * bmax + abs(beta) * cmax
+    vmax = float(np.abs(bias).max()) if (bias is not None and bias.size) else 0.0
+    scale = abs(alpha) * K * amax * bmax + abs(beta) * cmax + vmax
     d = float(diff.max())
     return d / scale if scale > 0 else (0.0 if d == 0 else float("inf"))
 
@@ -91,7 +94,8 @@ def make_inputs(M, N, K, dist="uniform", seed=0, beta=0.0, sigma_b=None):
 
 
 def run_checked(sg, A, B, C0, alpha, beta, *, kernel=None, lds=(None, None, None),
-                offsets=(0, 0, 0), tensor_cores=False, exact=False, rows=None):
+                offsets=(0, 0, 0), tensor_cores=False, exact=False, rows=None, bias=None,
+                act="none"):
     """One library call on padded device copies; checks the status, the kernel
     the library chose, canaries around all three operands, and parity with the
     oracle (bit-exact if `exact`, else the normwise gate).  Returns the error."""
@@ -110,7 +114,10 @@ def run_checked(sg, A, B, C0, alpha, beta, *, kernel=None, lds=(None, None, None
         chosen = sg.select_kernel(M, N, K, alpha, pa.view.data_ptr() or 0, pa.ld,
                                   pb.view.data_ptr() or 0, pb.ld, beta,
                                   pc.view.data_ptr() or 0, pc.ld, tensor_cores)
-        sg.sgemm(pa.view, pb.view, pc.view, alpha, beta, tensor_cores=tensor_cores)
+        import torch
+        dbias = torch.from_numpy(bias).cuda() if bias is not None else None
+        sg.sgemm(pa.view, pb.view, pc.view, alpha, beta, tensor_cores=tensor_cores, bias=dbias,
+                 activation=act)
         st = sg.status()
     finally:
         if prev is not None:
@@ -124,13 +131,16 @@ def run_checked(sg, A, B, C0, alpha, beta, *, kernel=None, lds=(None, None, None
     # the reduced-precision path is defined on TF32-rounded operands
     inputs = "tf32" if sg._mode(tensor_cores) == sg.MODE_TF32 else "fp32"
     Cref = oracle.sgemm(A, B, C0 if beta != 0.0 else None, alpha=alpha, beta=beta, rows=rows,
-                        inputs=inputs)
+                        inputs=inputs, bias=bias, act=act)
     got = C if rows is None else C[rows]
-    if exact or not use_ab:
+    # without the product, beta*C rounds once in both, so the result is exact;
+    # not with a bias (beta*C + bias rounds twice in FP32, once in the oracle)
+    # or after GELU / SiLU (FP32 tanhf / expf against fp64)
+    if exact or (not use_ab and bias is None and act in ("none", "relu")):
         assert np.array_equal(got.view(np.uint32), Cref.view(np.uint32)) or np.array_equal(got, Cref), \
             f"not bit-exact: max |diff| = {np.nanmax(np.abs(got - Cref)) if got.size else 0}"
         err = 0.0
     else:
-        err = normwise_err(got, Cref, A, B, K, alpha, beta, C0)
+        err = normwise_err(got, Cref, A, B, K, alpha, beta, C0, bias)
         assert err <= GATE, f"normwise error {err:.3e} above {GATE}"
     return err, chosen

@@ -323,6 +323,75 @@ def test_tf32x3_nan_propagates():
     assert np.isnan(C[7]).all() and np.isfinite(np.delete(C, 7, axis=0)).all()
 
 
+# ---------------------------------------------------------------- fused epilogue
+# C = act(alpha*A@B + beta*C + bias[j]) on every kernel path: the TMA tile
+# kernel (whole tiles and a split last wave), the plain-load kernel, the three
+# decode kernels, C = act(beta*C + bias) without the product, and both TF32
+# tensor-core kernels.
+EPI_CASES = [  # (M, N, K, kernel, tensor_cores, ldb padding)
+    (300, 260, 516, TMA, False, 0),        # 9 tiles, split along K
+    (1100, 700, 200, TMA, False, 0),       # whole tiles
+    (150, 130, 70, GEN, False, 3),
+    (16, 1000, 512, DEC, False, 0),        # outer-product decode kernel
+    (4, 1000, 700, DEC, False, 0),         # TMA decode kernel
+    (8, 999, 700, DEC, False, 3),          # direct-load decode kernel (B unaligned)
+    (256, 384, 200, sg.KERNEL_TF32X3, True, 0),
+    (256, 384, 200, sg.KERNEL_TF32, sg.MODE_TF32, 0),
+]
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu", "silu"])
+@pytest.mark.parametrize("M,N,K,kern,tc,pad", EPI_CASES)
+def test_fused_epilogue(M, N, K, kern, tc, pad, act):
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=M + N + K, beta=0.5)
+    bias = synth.matrix(1, N, seed=M + K, stream=3, dist="normal")[0] * 4
+    lds = (K, N + pad, N + 1) if pad else (None, None, None)
+    _, chosen = run_checked(sg, A, B, C0, 0.1, 0.5, tensor_cores=tc, bias=bias, act=act, lds=lds)
+    assert chosen == kern
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu", "silu"])
+def test_fused_epilogue_without_product(act):
+    M, N, K = 77, 130, 40
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=5, beta=1.0)
+    bias = synth.matrix(1, N, seed=6, stream=3, dist="normal")[0]
+    for alpha, k in ((0.0, K), (1.0, 0)):
+        run_checked(sg, A[:, :k], B[:k], C0, alpha, -0.75, bias=bias, act=act)
+
+
+def test_fused_epilogue_integers_exact_and_nan():
+    # small integers: alpha*A@B + beta*C + bias is exact in FP32, and ReLU keeps it exact
+    A, B, C0 = make_inputs(300, 260, 516, "int", seed=8, beta=1.0)
+    bias = synth.matrix(1, 260, seed=8, stream=3, dist="int")[0] * 16
+    run_checked(sg, A, B, C0, 2.0, -1.0, bias=bias, act="relu", exact=True)
+    run_checked(sg, A[:4], B, C0[:4], 2.0, -1.0, bias=bias, act="relu", exact=True)
+    # a NaN in C reaches the output through ReLU (not clamped to 0)
+    C1 = C0.copy()
+    C1[5, 7] = np.nan
+    dA, dB, dC = (torch.from_numpy(x).cuda() for x in (A, B, C1))
+    sg.sgemm(dA, dB, dC, 1.0, 1.0, bias=torch.from_numpy(bias).cuda(), activation="relu")
+    assert sg.status() == sg.OK
+    C = dC.cpu().numpy()
+    assert np.isnan(C[5, 7]) and np.isfinite(np.delete(C.reshape(-1), 5 * 260 + 7)).all()
+
+
+def test_fused_epilogue_rejects_bad_arguments():
+    dA = torch.randn(64, 32, device="cuda")
+    dB = torch.randn(32, 48, device="cuda")
+    dC = torch.zeros(64, 48, device="cuda")
+    L = sg.lib()
+    args = (64, 48, 32, 1.0, dA.data_ptr(), 32, dB.data_ptr(), 48, 0.0, dC.data_ptr(), 48)
+    assert L.sgemm_fused(*args, None, 4, 0, None) == sg.ERR_BAD_ARG          # activation
+    assert L.sgemm_fused(*args, None, 1, 3, None) == sg.ERR_BAD_ARG          # mode
+    assert L.sgemm_fused(*args, dC.data_ptr() + 4 * 48 * 10, 1, 0, None) == sg.ERR_ALIAS
+    with pytest.raises(ValueError):
+        sg.sgemm(dA, dB, dC, activation="tanh")
+    with pytest.raises(TypeError):
+        sg.sgemm(dA, dB, dC, bias=torch.zeros(47, device="cuda"))
+    torch.cuda.synchronize()
+    assert (dC == 0).all()
+
+
 # ---------------------------------------------------------------- 1xTF32 (sgemm_tf32)
 # The contract: A and B rounded to TF32 (nearest, ties away), then the FP32
 # product -- checked against the oracle on rounded operands at the FP32 gate.
