@@ -96,12 +96,21 @@ class Oracle:
         self.lib.oracle_max_threads.argtypes = []
         self.lib.oracle_round_tf32.restype = None
         self.lib.oracle_round_tf32.argtypes = [_f32p, _f32p, ctypes.c_int64]
+        self.lib.oracle_round_bf16.restype = None
+        self.lib.oracle_round_bf16.argtypes = [_f32p, _f32p, ctypes.c_int64]
 
     def round_tf32(self, x: np.ndarray) -> np.ndarray:
         """x rounded to TF32 (nearest, ties away from zero) as a new float32 array."""
         x = np.ascontiguousarray(x, dtype=np.float32)
         out = np.empty_like(x)
         self.lib.oracle_round_tf32(_ptr(x.reshape(-1)), _ptr(out.reshape(-1)), x.size)
+        return out
+
+    def round_bf16(self, x: np.ndarray) -> np.ndarray:
+        """x rounded to BF16 (nearest, ties to even) as a new float32 array."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty_like(x)
+        self.lib.oracle_round_bf16(_ptr(x.reshape(-1)), _ptr(out.reshape(-1)), x.size)
         return out
 
     def max_threads(self) -> int:
@@ -165,10 +174,13 @@ def sgemm(A, B, C0=None, alpha=1.0, beta=0.0, rows=None, threads=0, inputs="fp32
     """act(alpha*A@B + beta*C0 + bias) from the default oracle build (see
     ``Oracle.sgemm``).
 
-    ``inputs="tf32"`` gives the reduced-precision product: A and B are rounded
-    to TF32 first (``round_tf32``), C0 and bias are not."""
+    ``inputs="tf32"`` / ``"bf16"`` give the reduced-precision products: A and B
+    are rounded to TF32 / BF16 first (``round_tf32`` / ``round_bf16``), C0 and
+    bias are not."""
     if inputs == "tf32":
         A, B = round_tf32(A), round_tf32(B)
+    elif inputs == "bf16":
+        A, B = round_bf16(A), round_bf16(B)
     elif inputs != "fp32":
         raise ValueError(f"unknown input precision {inputs!r}")
     return default().sgemm(A, B, C0, alpha=alpha, beta=beta, rows=rows, threads=threads,
@@ -178,3 +190,8 @@ def sgemm(A, B, C0=None, alpha=1.0, beta=0.0, rows=None, threads=0, inputs="fp32
 def round_tf32(x):
     """x rounded to TF32, nearest with ties away from zero (see ``oracle_round_tf32``)."""
     return default().round_tf32(x)
+
+
+def round_bf16(x):
+    """x rounded to BF16, nearest with ties to even (see ``oracle_round_bf16``)."""
+    return default().round_bf16(x)

@@ -31,10 +31,10 @@
  * The loops run in i-k-j order: one double accumulator row per output row,
  * so each S[i][j] is still summed in ascending k.  OpenMP splits the rows.
  *
- * The reduced-precision product (the library's sgemm_tf32) is defined as the
- * same sum over operands first rounded to TF32 by oracle_round_tf32 below;
- * the caller rounds A and B and passes the rounded copies to the functions
- * above (C0 is not rounded).
+ * The reduced-precision products (the library's sgemm_tf32 and sgemm_bf16)
+ * are defined as the same sum over operands first rounded to TF32 or BF16 by
+ * oracle_round_tf32 / oracle_round_bf16 below; the caller rounds A and B and
+ * passes the rounded copies to the functions above (C0 is not rounded).
  */
 #include <math.h>
 #include <stdint.h>
@@ -203,6 +203,30 @@ void oracle_round_tf32(const float *x, float *out, int64_t n)
                 u |= 0x00400000u;
         } else {
             u = (u + 0x1000u) & 0xffffe000u;
+        }
+        memcpy(&out[i], &u, sizeof u);
+    }
+}
+
+/*
+ * BF16 keeps FP32's sign bit, its 8-bit exponent and the top 7 of its 23
+ * stored mantissa bits.  out[i] = x[i] rounded to the nearest BF16 value,
+ * ties to the value whose last kept bit is 0 (round to nearest even, the
+ * IEEE default).  On the bit pattern: add 0x7fff plus the last kept bit to
+ * the magnitude, then clear the 16 dropped bits.  Carries and overflow behave
+ * as for TF32 above; infinities are unchanged and a NaN stays a NaN.
+ * out[i] holds the BF16 value as a float (its low 16 bits zero).
+ */
+void oracle_round_bf16(const float *x, float *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        uint32_t u;
+        memcpy(&u, &x[i], sizeof u);
+        if ((u & 0x7f800000u) == 0x7f800000u) {
+            if (u & 0x007fffffu)
+                u |= 0x00400000u;
+        } else {
+            u = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;
         }
         memcpy(&out[i], &u, sizeof u);
     }

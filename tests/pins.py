@@ -254,6 +254,53 @@ def pin_tf32_nearest(orc):
     assert tie[:2000].all() and np.all(np.abs(rd[tie]) > np.abs(xd[tie])), "tie not away from zero"
 
 
+def pin_bf16_exact_cases(orc):
+    """BF16 rounding (7 stored mantissa bits, nearest, ties to even) on
+    hand-computed cases, including ties in both directions and the carry."""
+    u = 2.0 ** -23
+    cases = [
+        (1.0, 1.0),
+        (1.0 + 2.0 ** -7, 1.0 + 2.0 ** -7),                   # representable
+        (1.0 + 2.0 ** -8, 1.0),                               # tie, even neighbour below
+        (1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -6),               # tie, even neighbour above
+        (1.0 + 2.0 ** -8 + u, 1.0 + 2.0 ** -7),               # just above a tie
+        (1.0 + 3 * 2.0 ** -8 - u, 1.0 + 2.0 ** -7),           # just below a tie
+        (-(1.0 + 3 * 2.0 ** -8), -(1.0 + 2.0 ** -6)),         # negative tie, to even
+        (2.0 - u, 2.0),                                       # carry into the next binade
+        ((2.0 - 2.0 ** -7) * 2.0 ** 127, (2.0 - 2.0 ** -7) * 2.0 ** 127),   # largest BF16
+        (float(np.finfo(np.float32).max), np.inf),
+        (np.inf, np.inf), (-np.inf, -np.inf),
+    ]
+    x = np.array([c[0] for c in cases], dtype=np.float32)
+    want = np.array([c[1] for c in cases], dtype=np.float32)
+    assert np.array_equal(orc.round_bf16(x), want), (x, orc.round_bf16(x), want)
+    nan = orc.round_bf16(np.array([np.nan, _f32(0x7f800001)], dtype=np.float32))
+    assert np.all(np.isnan(nan))
+
+
+def pin_bf16_nearest(orc):
+    """Random normal floats: the result has 7 stored bits, is one of x's two
+    BF16 neighbours, the nearer in exact fp64 distance, and on a tie the one
+    whose last kept bit is 0."""
+    rng = _rng(98)
+    bits = rng.integers(0x00800000, 0x7f000000, size=200000, dtype=np.uint32)
+    bits |= rng.integers(0, 2, size=bits.size, dtype=np.uint32) << 31
+    bits[:2000] = (bits[:2000] & 0xffff0000) | 0x8000            # exact ties
+    x = bits.view(np.float32)
+    r = orc.round_bf16(x)
+    rb = r.view(np.uint32)
+    assert np.all((rb & 0xffff) == 0)
+    cut = (bits & 0xffff0000).view(np.float32).astype(np.float64)
+    e = np.floor(np.log2(np.abs(cut)))
+    up = cut + np.sign(cut) * np.exp2(e - 7)
+    xd, rd = x.astype(np.float64), r.astype(np.float64)
+    assert np.all((rd == cut) | (rd == up))
+    d_r, d_o = np.abs(xd - rd), np.abs(xd - np.where(rd == cut, up, cut))
+    assert np.all(d_r <= d_o)
+    tie = d_r == d_o
+    assert tie[:2000].all() and np.all(((rb[tie] >> 16) & 1) == 0), "tie not to even"
+
+
 def pin_bias_relu(orc):
     """Fused epilogue on small integers, exact in int64: the bias is per column
     (added to every row), ReLU clamps the sum below zero, and a NaN in C0
@@ -312,5 +359,5 @@ def pin_gelu_silu(orc):
 
 ALL_PINS = [pin_small_int_exact, pin_exact_rational, pin_identity, pin_permutation,
             pin_rank1, pin_transpose, pin_freivalds, pin_alpha_beta, pin_ld_gaps,
-            pin_row_subset, pin_tf32_exact_cases, pin_tf32_nearest, pin_bias_relu,
-            pin_gelu_silu]
+            pin_row_subset, pin_tf32_exact_cases, pin_tf32_nearest, pin_bf16_exact_cases,
+            pin_bf16_nearest, pin_bias_relu, pin_gelu_silu]

@@ -44,6 +44,9 @@ MUTANTS = [
     ("tf32_ties_even", "u = (u + 0x1000u) & 0xffffe000u;",
      "u = (u + 0x0fffu + ((u >> 13) & 1u)) & 0xffffe000u;"),
     ("tf32_keeps_11_bits", "u = (u + 0x1000u) & 0xffffe000u;", "u = (u + 0x0800u) & 0xfffff000u;"),
+    ("bf16_ties_away", "u = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;",
+     "u = (u + 0x8000u) & 0xffff0000u;"),
+    ("bf16_truncates", "u = (u + 0x7fffu + ((u >> 16) & 1u)) & 0xffff0000u;", "u = u & 0xffff0000u;"),
     ("bias_by_row", "v += (double)bias[j];", "v += (double)bias[i % N];"),
     ("act_before_bias", "orow[j] = (float)activate(v, act);",
      "orow[j] = (float)(activate(v - (bias ? (double)bias[j] : 0.0), act) + (bias ? (double)bias[j] : 0.0));"),
