@@ -335,6 +335,12 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3):
     out["sgemm_8192_tf32"] = {"shape": [8192, 8192, 8192], "kernel": kn, "ms": per, "ms_eager": pe,
                               "status": st, "TFLOP/s": tfl, "tf32_peak": tf32_peak,
                               "frac_tf32_peak": tfl / tf32_peak}
+    # BF16 path: operands rounded to BF16, against the measured bf16 GEMM peak
+    per, st, kn, pe = bench_shape(8192, 8192, 8192, 1.0, tensor_cores=sg.MODE_BF16)
+    tfl = 2 * 8192**3 / (per * 1e-3) / 1e12
+    out["sgemm_8192_bf16"] = {"shape": [8192, 8192, 8192], "kernel": kn, "ms": per, "ms_eager": pe,
+                              "status": st, "TFLOP/s": tfl, "bf16_peak": peaks["bf16_tflops"],
+                              "frac_bf16_peak": tfl / peaks["bf16_tflops"]}
     return out
 
 

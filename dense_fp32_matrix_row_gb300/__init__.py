@@ -15,7 +15,7 @@ import os
 
 from .build import LIBRARY, build  # noqa: F401  (build is part of the public API)
 
-__all__ = ["sgemm", "sgemm_3xtf32", "sgemm_tf32", "sgemm_ptr", "status", "select_kernel",
+__all__ = ["sgemm", "sgemm_3xtf32", "sgemm_tf32", "sgemm_bf16", "sgemm_ptr", "status", "select_kernel",
            "force_kernel", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
            "version", "SgemmError", "lib"]
 
@@ -25,15 +25,16 @@ ERR_CUDA, ERR_DEVICE, ERR_TIMEOUT, ERR_BAD_ARG = -5, -6, -7, -8
 ERR_TOO_LARGE, ERR_CAPTURE = -9, -10
 
 KERNEL_AUTO, KERNEL_NONE, KERNEL_SCALE_C, KERNEL_FFMA_TMA = 0, 1, 2, 3
-KERNEL_FFMA_GENERIC, KERNEL_DECODE, KERNEL_TF32X3, KERNEL_TF32 = 4, 5, 6, 7
+KERNEL_FFMA_GENERIC, KERNEL_DECODE, KERNEL_TF32X3, KERNEL_TF32, KERNEL_BF16 = 4, 5, 6, 7, 8
 KERNEL_NAMES = {KERNEL_NONE: "none", KERNEL_SCALE_C: "scale_c", KERNEL_FFMA_TMA: "ffma_tma",
                 KERNEL_FFMA_GENERIC: "ffma_generic", KERNEL_DECODE: "decode",
-                KERNEL_TF32X3: "tf32x3", KERNEL_TF32: "tf32"}
+                KERNEL_TF32X3: "tf32x3", KERNEL_TF32: "tf32", KERNEL_BF16: "bf16"}
 # activations of the fused epilogue (sgemm_fused)
 ACTIVATIONS = {"none": 0, "relu": 1, "gelu": 2, "silu": 3}
 # arithmetic of a call (sgemm, sgemm_3xtf32, sgemm_tf32)
-MODE_FP32, MODE_3XTF32, MODE_TF32 = 0, 1, 2
-_ENTRY = {MODE_FP32: "sgemm", MODE_3XTF32: "sgemm_3xtf32", MODE_TF32: "sgemm_tf32"}
+MODE_FP32, MODE_3XTF32, MODE_TF32, MODE_BF16 = 0, 1, 2, 3
+_ENTRY = {MODE_FP32: "sgemm", MODE_3XTF32: "sgemm_3xtf32", MODE_TF32: "sgemm_tf32",
+          MODE_BF16: "sgemm_bf16"}
 
 
 def _mode(tensor_cores) -> int:
@@ -68,7 +69,7 @@ def lib() -> ctypes.CDLL:
                 f"CUDA library {LIBRARY} is not built; run "
                 "`python -m dense_fp32_matrix_row_gb300.build` (there is no CPU fallback)")
         L = ctypes.CDLL(LIBRARY)
-        for name in ("sgemm", "sgemm_3xtf32", "sgemm_tf32"):
+        for name in ("sgemm", "sgemm_3xtf32", "sgemm_tf32", "sgemm_bf16"):
             getattr(L, name).argtypes = _GEMM_ARGS
             getattr(L, name).restype = ctypes.c_int
         L.sgemm_fused.argtypes = _GEMM_ARGS[:-1] + [_vp, ctypes.c_int, ctypes.c_int, _vp]
@@ -191,6 +192,12 @@ def sgemm_tf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> N
     """``sgemm`` on the reduced-precision 1xTF32 tensor-core path: A and B are
     rounded to TF32 first (see include/sgemm_gb300.h for the contract)."""
     sgemm(A, B, C, alpha, beta, stream, tensor_cores=MODE_TF32)
+
+
+def sgemm_bf16(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:
+    """``sgemm`` on the reduced-precision BF16 tensor-core path: A and B are
+    rounded to BF16 first (see include/sgemm_gb300.h for the contract)."""
+    sgemm(A, B, C, alpha, beta, stream, tensor_cores=MODE_BF16)
 
 
 def status(stream=None) -> int:

@@ -170,14 +170,16 @@ bool kernel_can_run(int id, int64_t M, int64_t N, int64_t K, const float *A, int
         case SGEMM_KERNEL_FFMA_GENERIC: return (M + 63) / 64 <= 65535;
         case SGEMM_KERNEL_DECODE: return M <= 16 && (N + 127) / 128 <= 65535;
         case SGEMM_KERNEL_TF32X3:
-        case SGEMM_KERNEL_TF32: return tf32x3_can_run(M, N, K);
+        case SGEMM_KERNEL_TF32:
+        case SGEMM_KERNEL_BF16: return tf32x3_can_run(M, N, K);
         default: return false;
     }
 }
 
 int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
            const float *B, int64_t ldb, float beta, const float *C, int64_t ldc, int mode) {
-    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32)
+    if (mode != SGEMM_MODE_FP32 && mode != SGEMM_MODE_3XTF32 && mode != SGEMM_MODE_TF32 &&
+        mode != SGEMM_MODE_BF16)
         return SGEMM_ERR_BAD_ARG;
     bool uses_ab = false;
     const int rc = check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, &uses_ab);
@@ -190,7 +192,9 @@ int choose(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t
     // The tensor-core tile is 128 rows tall; skinny products stay on the
     // (FP32-exact) decode kernel.
     if (mode != SGEMM_MODE_FP32 && M > 16) {
-        const int tc = mode == SGEMM_MODE_3XTF32 ? SGEMM_KERNEL_TF32X3 : SGEMM_KERNEL_TF32;
+        const int tc = mode == SGEMM_MODE_3XTF32 ? SGEMM_KERNEL_TF32X3
+                       : mode == SGEMM_MODE_TF32 ? SGEMM_KERNEL_TF32
+                                                 : SGEMM_KERNEL_BF16;
         if (kernel_can_run(tc, M, N, K, A, lda, B, ldb)) return tc;
     }
     if (M <= 16 && kernel_can_run(SGEMM_KERNEL_DECODE, M, N, K, A, lda, B, ldb))
@@ -250,8 +254,9 @@ int run(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t ld
             break;
         }
         case SGEMM_KERNEL_TF32X3:
-        case SGEMM_KERNEL_TF32: {
-            const int terms = kid == SGEMM_KERNEL_TF32X3 ? 3 : 1;
+        case SGEMM_KERNEL_TF32:
+        case SGEMM_KERNEL_BF16: {
+            const int terms = kid == SGEMM_KERNEL_TF32X3 ? 3 : kid == SGEMM_KERNEL_TF32 ? 1 : 0;
             float *ws = nullptr;
             const int rc =
                 workspace(tf32_workspace_floats(M, N, K, terms) * sizeof(float), g.stream, &ws);
@@ -276,6 +281,18 @@ bool encode_tma_2d(EncodeTiledFn enc, CUtensorMap *map, const float *base, int64
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+bool encode_tma_2d_bf16(EncodeTiledFn enc, CUtensorMap *map, const void *base, int64_t inner,
+                        int64_t rows, int64_t ld, uint32_t box_inner, uint32_t box_rows,
+                        CUtensorMapSwizzle swz) {
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -331,6 +348,11 @@ int sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int
     return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, SGEMM_MODE_TF32);
 }
 
+int sgemm_bf16(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
+               const float *B, int64_t ldb, float beta, float *C, int64_t ldc, void *stream) {
+    return run(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream, SGEMM_MODE_BF16);
+}
+
 int sgemm_fused(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int64_t lda,
                 const float *B, int64_t ldb, float beta, float *C, int64_t ldc, const float *bias,
                 int activation, int mode, void *stream) {
@@ -383,7 +405,8 @@ int sgemm_select_kernel(int64_t M, int64_t N, int64_t K, float alpha, const floa
 
 int sgemm_force_kernel(int id) {
     if (id != SGEMM_KERNEL_AUTO && id != SGEMM_KERNEL_FFMA_TMA && id != SGEMM_KERNEL_FFMA_GENERIC &&
-        id != SGEMM_KERNEL_DECODE && id != SGEMM_KERNEL_TF32X3 && id != SGEMM_KERNEL_TF32)
+        id != SGEMM_KERNEL_DECODE && id != SGEMM_KERNEL_TF32X3 && id != SGEMM_KERNEL_TF32 &&
+        id != SGEMM_KERNEL_BF16)
         return SGEMM_ERR_BAD_ARG;
     return g_force.exchange(id);
 }

@@ -53,6 +53,10 @@ struct GemmArgs {
 bool encode_tma_2d(EncodeTiledFn enc, CUtensorMap *map, const float *base, int64_t inner,
                    int64_t rows, int64_t ld, uint32_t box_inner, uint32_t box_rows,
                    CUtensorMapSwizzle swz);
+// The same over 16-bit BF16 elements (ld and the box in elements).
+bool encode_tma_2d_bf16(EncodeTiledFn enc, CUtensorMap *map, const void *base, int64_t inner,
+                        int64_t rows, int64_t ld, uint32_t box_inner, uint32_t box_rows,
+                        CUtensorMapSwizzle swz);
 
 // ---- launchers (one translation unit each) ------------------------------------
 cudaError_t launch_scale_c(const GemmArgs &g);
@@ -80,12 +84,20 @@ cudaError_t launch_transpose_split(int64_t K, int64_t N, const float *B, int64_t
 // (lo == nullptr: the rounded hi part only).
 cudaError_t launch_split_rows(int64_t R, int64_t Cc, const float *X, int64_t ldx, float *hi,
                               float *lo, int64_t ldo, cudaStream_t stream);
+// BF16 (round to nearest even) copies for the BF16 tensor-core kernel:
+// out[r*ldo + c] = bf16(X[r][c]) and out[n*ldo + k] = bf16(B[k][n]); `out` is
+// bf16 storage, ldo in elements, a multiple of 4.
+cudaError_t launch_bf16_rows(int64_t R, int64_t Cc, const float *X, int64_t ldx, void *out,
+                             int64_t ldo, cudaStream_t stream);
+cudaError_t launch_bf16_transpose(int64_t K, int64_t N, const float *B, int64_t ldb, void *out,
+                                  int64_t ldo, cudaStream_t stream);
 cudaError_t launch_decode(const GemmArgs &g);
 cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t stream);
-// TF32 tensor-core kernels.  terms == 3 (3xTF32): splits A and B into TF32
+// Tensor-core kernels.  terms == 3 (3xTF32): splits A and B into TF32
 // hi/lo parts in `workspace`, then accumulates hi*lo + lo*hi + hi*hi with
 // tcgen05 MMAs.  terms == 1 (1xTF32): rounds A and B to TF32 (the hi parts
-// only) and accumulates hi*hi.  The workspace holds
+// only) and accumulates hi*hi.  terms == 0 (BF16): rounds A and B to BF16
+// and accumulates their products (kind::f16).  The workspace holds
 // tf32_workspace_floats(M, N, K, terms) floats.
 cudaError_t launch_tf32(const GemmArgs &g, float *workspace, int terms);
 size_t tf32_workspace_floats(int64_t M, int64_t N, int64_t K, int terms);

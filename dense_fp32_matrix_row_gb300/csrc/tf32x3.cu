@@ -27,6 +27,8 @@
 // Every wait is bounded.  On a time-out the kernel records the error, waits
 // (bounded) for its own TMA copies and MMAs in flight, frees its tensor
 // memory and exits without storing.
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace sgemm_gb300 {
@@ -45,14 +47,23 @@ constexpr uint32_t TMEM_COLS = 2 * TBN;                    // two 128 x 256 FP32
 
 // Per-stage layout: the A parts, then the B parts (hi, then lo for 3 terms).
 // 3 terms: 48 KB stages, 4 deep; 1 term: 24 KB stages, 8 deep (192 KB both).
-template <int TERMS>
+// Operand kinds: FP32 bit patterns read as TF32 (kind::tf32), or BF16
+// (kind::f16 with both operands BF16).
+enum : int { kTf32 = 0, kBf16 = 1 };
+
+template <int TERMS, int KIND = kTf32>
 struct TfCfg {
     static constexpr int PARTS = TERMS == 3 ? 2 : 1;
     static constexpr uint32_t STAGE_BYTES = PARTS * (A_TILE + B_TILE);
     static constexpr int TSTG = TERMS == 3 ? 4 : 8;
     static constexpr size_t SMEM = 1024 + (size_t)TSTG * STAGE_BYTES + 256;
+    // K elements in one 64-byte row of a tile, and per MMA instruction
+    static constexpr int KT = KIND == kTf32 ? TBK : 2 * TBK;
+    static constexpr int MMA_K = KIND == kTf32 ? 8 : 16;
     static_assert(TERMS == 1 || TERMS == 3, "1xTF32 or 3xTF32");
+    static_assert(KIND == kTf32 || TERMS == 1, "BF16 is one term");
     static_assert(SMEM <= 227 * 1024, "shared memory per block");
+    static_assert(KT / MMA_K == 2, "two MMAs of 32 bytes of K per 64-byte row");
 };
 constexpr uint64_t DRAIN_NS = 1000000000ull;
 static_assert(TBK * 4 == 64, "rows of a K slice fill exactly one 64-byte swizzle span");
@@ -64,6 +75,11 @@ static_assert(EPI_WARPS % 4 == 0 && EPI_COLS % 16 == 0, "epilogue covers all lan
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 constexpr uint32_t IDESC = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(TBN >> 3) << 17) |
                            ((uint32_t)(TBM >> 4) << 24);
+// kind::f16 with BF16 operands: the same fields, A and B format BF16 (1),
+// both taken from one constant so that they can never differ.
+constexpr uint32_t BF16_FORMAT = 1;
+constexpr uint32_t IDESC_BF16 = (1u << 4) | (BF16_FORMAT << 7) | (BF16_FORMAT << 10) |
+                                ((uint32_t)(TBN >> 3) << 17) | ((uint32_t)(TBM >> 4) << 24);
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with the 64-byte swizzle: rows of 64 bytes, 8-row core groups 512 bytes
@@ -95,6 +111,16 @@ __device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(IDESC_BF16), "r"(accumulate)
+        : "memory");
+}
+
 // The mbarrier completes once every tcgen05 operation this thread issued so far is done.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -123,14 +149,15 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 // thread therefore restarts the accumulator every KC_TILES k-tiles, in two
 // alternating tensor-memory buffers, and the epilogue warps add each chunk
 // into FP32 registers (round to nearest) while the next chunk is computed.
-template <int TERMS>
+template <int TERMS, int KIND>
 __global__ void __launch_bounds__(THREADS, 1)
 tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
                 const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
                 int M, int N, int K, Epilogue ep, float *__restrict__ C, int64_t ldc,
                 int c_vec4, unsigned *err, uint64_t wait_ns) {
-    using L = TfCfg<TERMS>;
+    using L = TfCfg<TERMS, KIND>;
     constexpr int TSTG = L::TSTG;
+    constexpr int KT = L::KT;
     constexpr uint32_t STAGE_BYTES = L::STAGE_BYTES;
     extern __shared__ unsigned char smem_raw[];
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
@@ -153,7 +180,7 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
     const int tile_m = first_m + (pid % per_group) % gsz;
     const int tile_n = (pid % per_group) / gsz;
     const int m0 = tile_m * TBM, n0 = tile_n * TBN;
-    const int ktiles = (K + TBK - 1) / TBK;
+    const int ktiles = (K + KT - 1) / KT;
     const int nchunks = (ktiles + KC_TILES - 1) / KC_TILES;
     auto stage_ptr = [&](int s, int which) -> uint32_t {   // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
         constexpr int P = L::PARTS;
@@ -201,11 +228,11 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                 if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, wait_ns)) break;
                 const uint32_t fb = smem_u32(&full[s]);
                 mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                tma_load_2d(stage_ptr(s, 0), &tmAhi, fb, kt * TBK, m0);
-                tma_load_2d(stage_ptr(s, 2), &tmBhi, fb, kt * TBK, n0);
+                tma_load_2d(stage_ptr(s, 0), &tmAhi, fb, kt * KT, m0);
+                tma_load_2d(stage_ptr(s, 2), &tmBhi, fb, kt * KT, n0);
                 if (TERMS == 3) {
-                    tma_load_2d(stage_ptr(s, 1), &tmAlo, fb, kt * TBK, m0);
-                    tma_load_2d(stage_ptr(s, 3), &tmBlo, fb, kt * TBK, n0);
+                    tma_load_2d(stage_ptr(s, 1), &tmAlo, fb, kt * KT, m0);
+                    tma_load_2d(stage_ptr(s, 3), &tmBlo, fb, kt * KT, n0);
                 }
             }
             if (kt < ktiles) {
@@ -237,8 +264,8 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < TBK / 8; ++kk) {
-                        const uint32_t koff = kk * 32;   // 8 TF32 = 32 bytes along K
+                    for (int kk = 0; kk < KT / L::MMA_K; ++kk) {
+                        const uint32_t koff = kk * 32;   // 8 TF32 or 16 BF16 = 32 bytes along K
                         const uint64_t ahi = smem_desc_sw64(stage_ptr(s, 0) + koff);
                         const uint64_t bhi = smem_desc_sw64(stage_ptr(s, 2) + koff);
                         const uint32_t acc_in = (kt != c * KC_TILES || kk != 0) ? 1u : 0u;
@@ -248,6 +275,8 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                             tc_mma_tf32(d, ahi, blo, acc_in);
                             tc_mma_tf32(d, alo, bhi, 1u);
                             tc_mma_tf32(d, ahi, bhi, 1u);
+                        } else if (KIND == kBf16) {
+                            tc_mma_bf16(d, ahi, bhi, acc_in);
                         } else {
                             tc_mma_tf32(d, ahi, bhi, acc_in);
                         }
@@ -355,6 +384,25 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
 
 int64_t tf32_ld(int64_t K) { return (K + 3) / 4 * 4; }
 
+template <int TERMS, int KIND>
+cudaError_t launch_mma(const GemmArgs &g, const CUtensorMap &tAhi, const CUtensorMap &tAlo,
+                       const CUtensorMap &tBhi, const CUtensorMap &tBlo) {
+    using L = TfCfg<TERMS, KIND>;
+    cudaError_t e = cudaFuncSetAttribute(tf32_mma_kernel<TERMS, KIND>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = ((g.N + TBN - 1) / TBN) * ((g.M + TBM - 1) / TBM);
+    if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)tiles);
+    const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
+    tf32_mma_kernel<TERMS, KIND><<<grid, THREADS, L::SMEM, g.stream>>>(
+        tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N, (int)g.K, g.epi(), g.C, g.ldc, c_vec4,
+        g.err, g.wait_ns);
+    return cudaGetLastError();
+}
+
+int64_t bf16_ld(int64_t K) { return (K + 7) / 8 * 8; }
+
 template <int TERMS>
 cudaError_t launch_terms(const GemmArgs &g, float *ws) {
     using L = TfCfg<TERMS>;
@@ -384,22 +432,36 @@ cudaError_t launch_terms(const GemmArgs &g, float *ws) {
         tAlo = tAhi;   // never read
         tBlo = tBhi;
     }
-    e = cudaFuncSetAttribute(tf32_mma_kernel<TERMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)L::SMEM);
+    return launch_mma<TERMS, kTf32>(g, tAhi, tAlo, tBhi, tBlo);
+}
+
+// BF16: A and B^T rounded to BF16 (nearest even) as [M][ldk] and [N][ldk]
+// 16-bit arrays, ldk = K rounded up to 8 (16-byte rows).
+cudaError_t launch_bf16_terms(const GemmArgs &g, float *ws) {
+    const int64_t ldk = bf16_ld(g.K);
+    const int64_t asz = (g.M * ldk + 127) / 128 * 128, bsz = (g.N * ldk + 127) / 128 * 128;
+    __nv_bfloat16 *a = reinterpret_cast<__nv_bfloat16 *>(ws), *b = a + asz;
+    cudaError_t e = launch_bf16_rows(g.M, g.K, g.A, g.lda, a, ldk, g.stream);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = ((g.N + TBN - 1) / TBN) * ((g.M + TBM - 1) / TBM);
-    if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const dim3 grid((unsigned)tiles);
-    const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
-    tf32_mma_kernel<TERMS><<<grid, THREADS, L::SMEM, g.stream>>>(
-        tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N, (int)g.K, g.epi(), g.C, g.ldc, c_vec4,
-        g.err, g.wait_ns);
-    return cudaGetLastError();
+    e = launch_bf16_transpose(g.K, g.N, g.B, g.ldb, b, ldk, g.stream);
+    if (e != cudaSuccess) return e;
+    alignas(64) CUtensorMap tA, tB;
+    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
+    constexpr uint32_t kt = TfCfg<1, kBf16>::KT;
+    if (!encode_tma_2d_bf16(g.encode, &tA, a, g.K, g.M, ldk, kt, TBM, sw) ||
+        !encode_tma_2d_bf16(g.encode, &tB, b, g.K, g.N, ldk, kt, TBN, sw))
+        return cudaErrorInvalidValue;
+    return launch_mma<1, kBf16>(g, tA, tA, tB, tB);
 }
 
 }  // namespace
 
 size_t tf32_workspace_floats(int64_t M, int64_t N, int64_t K, int terms) {
+    if (terms == 0) {   // BF16: two 16-bit arrays
+        const int64_t ldk = bf16_ld(K);
+        const int64_t a = (M * ldk + 127) / 128 * 128, b = (N * ldk + 127) / 128 * 128;
+        return (size_t)((a + b) / 2);
+    }
     const int64_t ldk = tf32_ld(K);
     const int64_t a = (M * ldk + 63) / 64 * 64, b = (N * ldk + 63) / 64 * 64;
     return (size_t)((terms == 3 ? 2 : 1) * (a + b));
@@ -414,6 +476,7 @@ bool tf32x3_can_run(int64_t M, int64_t N, int64_t K) {
 cudaError_t launch_tf32(const GemmArgs &g, float *ws, int terms) {
     if (terms == 3) return launch_terms<3>(g, ws);
     if (terms == 1) return launch_terms<1>(g, ws);
+    if (terms == 0) return launch_bf16_terms(g, ws);
     return cudaErrorInvalidValue;
 }
 

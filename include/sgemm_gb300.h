@@ -79,6 +79,7 @@ extern "C" {
 #define SGEMM_KERNEL_DECODE        5   /* split-K streaming kernel for M <= 16 */
 #define SGEMM_KERNEL_TF32X3        6   /* 3xTF32 tensor-core kernel (sgemm_3xtf32) */
 #define SGEMM_KERNEL_TF32          7   /* 1xTF32 tensor-core kernel (sgemm_tf32) */
+#define SGEMM_KERNEL_BF16          8   /* BF16 tensor-core kernel (sgemm_bf16) */
 
 /* Activations of sgemm_fused's epilogue. */
 #define SGEMM_ACT_NONE   0   /* identity */
@@ -90,6 +91,7 @@ extern "C" {
 #define SGEMM_MODE_FP32    0   /* sgemm() */
 #define SGEMM_MODE_3XTF32  1   /* sgemm_3xtf32() */
 #define SGEMM_MODE_TF32    2   /* sgemm_tf32() */
+#define SGEMM_MODE_BF16    3   /* sgemm_bf16() */
 
 /*
  * sgemm -- C <- alpha * A @ B + beta * C in FP32 (FFMA) arithmetic.
@@ -164,6 +166,26 @@ int sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha,
                float beta, float *C, int64_t ldc, void *stream);
 
 /*
+ * sgemm_bf16 -- reduced-precision product on the BF16 tensor cores (opt-in).
+ *
+ * Accuracy contract: A and B are first rounded to BF16 (FP32's sign and
+ * exponent, 7 stored mantissa bits; round to nearest, ties to even), and the
+ * result is the FP32-accumulated product of the rounded operands,
+ * C = alpha * round(A) @ round(B) + beta * C; against that definition it
+ * meets sgemm()'s FP32 accuracy.  Against the unrounded product the error is
+ * that of the input rounding, up to 2^-8 relative per operand.  Operands
+ * that are already BF16 values (small integers, for instance) give the exact
+ * FP32 product.  C is not rounded.
+ * The operands are rounded into a workspace first (A as [M][K], B transposed
+ * to [N][K], 16-bit: (M+N)*round_up(K,8)/2 floats), so any alignment and ld
+ * are accepted.  Skinny products (M <= 16) run sgemm()'s FP32 decode kernel.
+ * Arguments, conventions and errors are those of sgemm().
+ */
+int sgemm_bf16(int64_t M, int64_t N, int64_t K, float alpha,
+               const float *A, int64_t lda, const float *B, int64_t ldb,
+               float beta, float *C, int64_t ldc, void *stream);
+
+/*
  * sgemm_fused -- sgemm() with the epilogue extended by a bias and an
  * activation, applied to each output before it is stored:
  *
@@ -177,8 +199,9 @@ int sgemm_tf32(int64_t M, int64_t N, int64_t K, float alpha,
  *   bias        device pointer to N floats (one per column), or NULL for none;
  *               must not overlap C (SGEMM_ERR_ALIAS)
  *   activation  SGEMM_ACT_*; anything else is SGEMM_ERR_BAD_ARG
- *   mode        SGEMM_MODE_*: the arithmetic of sgemm(), sgemm_3xtf32() or
- *               sgemm_tf32(), with the same kernels and accuracy contracts
+ *   mode        SGEMM_MODE_*: the arithmetic of sgemm(), sgemm_3xtf32(),
+ *               sgemm_tf32() or sgemm_bf16(), with the same kernels and
+ *               accuracy contracts
  * alpha*acc + beta*C + bias is formed in FP32 and the activation applied in
  * FP32 with CUDA's tanhf / expf.  When K == 0 or alpha == 0 the result is
  * act(beta * C + bias), A and B unread.  Other arguments, conventions and
@@ -204,8 +227,8 @@ const char *sgemm_status_string(int status);
  * sgemm_select_kernel -- which SGEMM_KERNEL_* sgemm() would run for these
  * arguments (host-only, launches nothing, needs no GPU).  Returns a negative
  * status code for arguments sgemm() would reject.  `mode` is one of
- * SGEMM_MODE_*: the choice of sgemm(), sgemm_3xtf32() or sgemm_tf32();
- * SGEMM_ERR_BAD_ARG for any other value.
+ * SGEMM_MODE_*: the choice of sgemm(), sgemm_3xtf32(), sgemm_tf32() or
+ * sgemm_bf16(); SGEMM_ERR_BAD_ARG for any other value.
  */
 int sgemm_select_kernel(int64_t M, int64_t N, int64_t K, float alpha,
                         const float *A, int64_t lda, const float *B, int64_t ldb,

@@ -129,7 +129,7 @@ def run_checked(sg, A, B, C0, alpha, beta, *, kernel=None, lds=(None, None, None
     assert pa.unchanged() and pb.unchanged(), "A or B was modified"
     use_ab = alpha != 0.0 and K > 0
     # the reduced-precision path is defined on TF32-rounded operands
-    inputs = "tf32" if sg._mode(tensor_cores) == sg.MODE_TF32 else "fp32"
+    inputs = {sg.MODE_TF32: "tf32", sg.MODE_BF16: "bf16"}.get(sg._mode(tensor_cores), "fp32")
     Cref = oracle.sgemm(A, B, C0 if beta != 0.0 else None, alpha=alpha, beta=beta, rows=rows,
                         inputs=inputs, bias=bias, act=act)
     got = C if rows is None else C[rows]

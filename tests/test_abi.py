@@ -96,10 +96,11 @@ def test_tensor_core_modes(L):
     assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=True) == sg.KERNEL_TF32X3
     assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=sg.MODE_3XTF32) == sg.KERNEL_TF32X3
     assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=sg.MODE_TF32) == sg.KERNEL_TF32
+    assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=sg.MODE_BF16) == sg.KERNEL_BF16
     # any alignment: both tensor-core paths read rounded / split copies
     assert sel(256, 130, 127, A=a + 4, B=b + 8, C=c, tensor_cores=sg.MODE_TF32) == sg.KERNEL_TF32
     # skinny products stay on the FP32 decode kernel in every mode
-    for mode in (sg.MODE_FP32, sg.MODE_3XTF32, sg.MODE_TF32):
+    for mode in (sg.MODE_FP32, sg.MODE_3XTF32, sg.MODE_TF32, sg.MODE_BF16):
         assert sel(16, 14336, 4096, A=a, B=b, C=c, tensor_cores=mode) == sg.KERNEL_DECODE
     assert sel(256, 256, 256, A=a, B=b, C=c, tensor_cores=sg.MODE_FP32) == sg.KERNEL_FFMA_TMA
     # an unknown mode is an argument error in the C ABI

@@ -25,7 +25,8 @@ import oracle  # noqa: E402
 
 @pytest.mark.parametrize("M,N,K,tc", [(16, 14336, 4096, False), (4, 1000, 700, False),
                                       (1000, 1000, 1000, False), (300, 516, 260, False),
-                                      (256, 512, 384, True), (256, 512, 384, sg.MODE_TF32)])
+                                      (256, 512, 384, True), (256, 512, 384, sg.MODE_TF32),
+                                      (256, 512, 384, sg.MODE_BF16)])
 def test_capture_and_replay(M, N, K, tc):
     A, B, C0 = make_inputs(M, N, K, "normal", seed=M + N + K, beta=0.5)
     s = torch.cuda.Stream()
@@ -47,7 +48,7 @@ def test_capture_and_replay(M, N, K, tc):
     assert sg.status(s) == sg.OK
     got = dC.cpu().numpy()
     assert np.array_equal(got, eager.cpu().numpy()), "replay differs from the eager call"
-    inputs = "tf32" if tc is sg.MODE_TF32 else "fp32"
+    inputs = {sg.MODE_TF32: "tf32", sg.MODE_BF16: "bf16"}.get(sg._mode(tc), "fp32")
     ref = oracle.sgemm(A, B, C0, alpha=1.25, beta=0.5, inputs=inputs)
     assert normwise_err(got, ref, A, B, K, 1.25, 0.5, C0) <= GATE
     # a second replay reads the operands' new contents

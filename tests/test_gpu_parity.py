@@ -337,6 +337,7 @@ EPI_CASES = [  # (M, N, K, kernel, tensor_cores, ldb padding)
     (8, 999, 700, DEC, False, 3),          # direct-load decode kernel (B unaligned)
     (256, 384, 200, sg.KERNEL_TF32X3, True, 0),
     (256, 384, 200, sg.KERNEL_TF32, sg.MODE_TF32, 0),
+    (256, 384, 200, sg.KERNEL_BF16, sg.MODE_BF16, 0),
 ]
 
 
@@ -382,7 +383,7 @@ def test_fused_epilogue_rejects_bad_arguments():
     L = sg.lib()
     args = (64, 48, 32, 1.0, dA.data_ptr(), 32, dB.data_ptr(), 48, 0.0, dC.data_ptr(), 48)
     assert L.sgemm_fused(*args, None, 4, 0, None) == sg.ERR_BAD_ARG          # activation
-    assert L.sgemm_fused(*args, None, 1, 3, None) == sg.ERR_BAD_ARG          # mode
+    assert L.sgemm_fused(*args, None, 1, 4, None) == sg.ERR_BAD_ARG          # mode
     assert L.sgemm_fused(*args, dC.data_ptr() + 4 * 48 * 10, 1, 0, None) == sg.ERR_ALIAS
     with pytest.raises(ValueError):
         sg.sgemm(dA, dB, dC, activation="tanh")
@@ -462,6 +463,77 @@ def test_workload_8192_tf32_sampled_rows():
     _, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"], tensor_cores=sg.MODE_TF32,
                             rows=_sample_rows(w["M"]))
     assert chosen == TF1
+
+
+# ---------------------------------------------------------------- BF16 (sgemm_bf16)
+# The contract: A and B rounded to BF16 (nearest, ties to even), then the FP32
+# product -- checked against the oracle on rounded operands at the FP32 gate.
+BF = sg.KERNEL_BF16
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 8, 8), (128, 256, 32), (129, 257, 40), (300, 520, 1000),
+                                   (1000, 1000, 1000), (257, 300, 4097)])
+def test_bf16_shapes(M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "uniform", seed=M * 3 + N + K, beta=0.5)
+    _, chosen = run_checked(sg, A, B, C0, 1.25, 0.5, tensor_cores=sg.MODE_BF16)
+    assert chosen == BF
+
+
+def test_bf16_small_integers_exact_and_layouts():
+    A, B, C0 = make_inputs(300, 200, 1000, "int", seed=7, beta=-2.0)
+    run_checked(sg, A, B, C0, 3.0, -2.0, tensor_cores=sg.MODE_BF16, exact=True)
+    A, B, C0 = make_inputs(70, 45, 33, "int", seed=14, beta=1.0)
+    for lds, offsets in [((37, 47, 46), (1, 3, 1)), ((40, 48, 48), (0, 0, 0))]:
+        run_checked(sg, A, B, C0, -1.0, 0.5, lds=lds, offsets=offsets,
+                    tensor_cores=sg.MODE_BF16, exact=True)
+
+
+def test_bf16_rounding_matches_the_oracle():
+    """B = I gives round(A) exactly (A = I gives round(B)): the GPU's BF16
+    rounding against the oracle's, including ties in both directions."""
+    import oracle
+    n = 256
+    rng = np.random.default_rng(12)
+    A = rng.standard_normal((n, n)).astype(np.float32) * 3
+    bits = A.view(np.uint32)
+    bits[:64] = (bits[:64] & 0xffff0000) | 0x8000                # exact ties
+    bits[64:96] = (bits[64:96] & 0xffff0000) | 0x7fff            # just below
+    bits[96:128] = (bits[96:128] & 0xffff0000) | 0x8001          # just above
+    eye = np.eye(n, dtype=np.float32)
+    want = oracle.round_bf16(A)
+    for X, Y in ((A, eye), (eye, A)):
+        dX, dY = torch.from_numpy(X).cuda(), torch.from_numpy(Y).cuda()
+        dC = torch.empty((n, n), device="cuda")
+        sg.sgemm_bf16(dX, dY, dC)
+        assert sg.status() == sg.OK
+        got = dC.cpu().numpy()
+        bad = np.flatnonzero(got.view(np.uint32) != want.view(np.uint32))
+        assert bad.size == 0, f"{bad.size} elements differ, first {got.flat[bad[0]]!r} vs {want.flat[bad[0]]!r}"
+
+
+def test_bf16_is_bf16():
+    """Within the FP32 gate of the product of BF16-rounded operands, and far
+    from both the exact product and the TF32-rounded one."""
+    from gpu_util import normwise_err
+    import oracle
+    M, N, K = 256, 256, 2048
+    A, B, _ = make_inputs(M, N, K, "uniform", seed=79)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.empty((M, N), device="cuda")
+    sg.sgemm_bf16(dA, dB, dC)
+    assert sg.status() == sg.OK
+    got = dC.cpu().numpy()
+    assert normwise_err(got, oracle.sgemm(A, B, inputs="bf16"), A, B, K) <= GATE
+    assert normwise_err(got, oracle.sgemm(A, B), A, B, K) > 30 * GATE
+    assert normwise_err(got, oracle.sgemm(A, B, inputs="tf32"), A, B, K) > 30 * GATE
+
+
+def test_workload_8192_bf16_sampled_rows():
+    A, B, C0, w = synth.workload_inputs("sgemm_8192")
+    C0 = np.full((w["M"], w["N"]), np.nan, np.float32)
+    _, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"], tensor_cores=sg.MODE_BF16,
+                            rows=_sample_rows(w["M"]))
+    assert chosen == BF
 
 
 def test_workload_8192_3xtf32_sampled_rows():
