@@ -44,6 +44,10 @@ L2_BYTES = 129 * 10**6
 # cuBLAS", results table).  Another machine: context, not the target.
 PAGES_BEST_TFLOPS = 23.2496
 
+# --mode names -> the binding's arithmetic mode
+MODES = {"fp32": lambda sg: sg.MODE_FP32, "3xtf32": lambda sg: sg.MODE_3XTF32,
+         "tf32": lambda sg: sg.MODE_TF32, "bf16": lambda sg: sg.MODE_BF16}
+
 KERNEL_SOURCES = {
     "ffma_tma": ["dense_fp32_matrix_row_gb300/csrc/ffma_tma.cu",
                  "dense_fp32_matrix_row_gb300/csrc/transpose.cu",
@@ -367,11 +371,14 @@ def run_ours(args, world, rank, local):
     dA = torch.from_numpy(A).to(dev)
     dB = torch.from_numpy(B).to(dev)
     dC = torch.from_numpy(C0).to(dev) if C0 is not None else torch.empty((M, N), device=dev)
-    tc = bool(args.tensor_cores)
+    mode_name = args.mode or ("3xtf32" if args.tensor_cores else "fp32")
+    tc = MODES[mode_name](sg)
     kid = sg.select_kernel(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta,
                            dC.data_ptr(), N, tc)
-    # kernels one sgemm() call launches: the FFMA path transposes A first
-    launches_per_call = {sg.KERNEL_FFMA_TMA: 2, sg.KERNEL_TF32X3: 3}.get(kid, 1)
+    # kernels one sgemm() call launches: the FFMA path transposes A first, the
+    # tensor-core paths convert A and B first
+    launches_per_call = {sg.KERNEL_FFMA_TMA: 2, sg.KERNEL_TF32X3: 3, sg.KERNEL_TF32: 3,
+                         sg.KERNEL_BF16: 3}.get(kid, 1)
 
     def step():
         sg.sgemm(dA, dB, dC, alpha, beta, stream=stream, tensor_cores=tc)
@@ -386,7 +393,8 @@ def run_ours(args, world, rank, local):
     if rank == 0 and not args.no_parity:
         import oracle
         rows = np.unique(np.r_[np.arange(0, M, 61), [M - 1]])
-        ref = oracle.sgemm(A, B, C0, alpha=alpha, beta=beta, rows=rows)
+        ref = oracle.sgemm(A, B, C0, alpha=alpha, beta=beta, rows=rows,
+                           inputs={"tf32": "tf32", "bf16": "bf16"}.get(mode_name, "fp32"))
         got = dC.cpu().numpy()[rows]
         err = float(np.abs(got.astype(np.float64) - ref).max() / (K * np.abs(A).max() * np.abs(B).max()))
         parity = {"rows_checked": int(rows.size), "normwise_err": err, "gate": 1e-6,
@@ -457,6 +465,18 @@ def run_ours(args, world, rank, local):
     props = torch.cuda.get_device_properties(dev)
     peak = acc.ffma_peak_tflops(props.multi_processor_count, float(peaks.get("sm_max_mhz", 2070.0)))
     achieved = flops / (per_launch_ms * 1e-3) / 1e12
+    bound, peak_source = "alu", (f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 FLOP x "
+                                 f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz ({peaks['_source']} max clock)")
+    if kid in (sg.KERNEL_TF32X3, sg.KERNEL_TF32, sg.KERNEL_BF16):
+        # tensor work against the tensor peak of the operand type
+        bound = "tensor"
+        if kid == sg.KERNEL_BF16:
+            peak, peak_source = peaks["bf16_tflops"], "measured bf16 GEMM burst"
+        else:
+            peak = acc.tf32_peak_from_bf16(peaks["bf16_tflops"])
+            peak_source = "measured bf16 GEMM burst x 1.1/2.25 (nominal TF32/BF16 ratio)"
+        if kid == sg.KERNEL_TF32X3:
+            achieved *= 3      # three TF32 products per useful product
     traffic = ncu_traffic("ffma_tma", name) if kid == sg.KERNEL_FFMA_TMA else None
     cpu = None
     if not args.no_cpu_baseline:
@@ -472,15 +492,13 @@ def run_ours(args, world, rank, local):
         "vs_baseline": value / PAGES_BEST_TFLOPS,
         "vs_baseline_ref": "pages' cuBLAS FP32 on an RTX A6000 at 4092^3 (23.25 TFLOP/s): "
                            "another machine, context only",
-        "dtype": "f32", "data": "synthetic",
+        "dtype": {"tf32": "tf32", "bf16": "bf16"}.get(mode_name, "f32"), "data": "synthetic",
         "config": workload_config(name, w, {
             "kernel": sg.KERNEL_NAMES.get(kid, str(kid)),
             "l2": f"operands {4 * (M * K + K * N + M * N) / 1e6:.0f} MB > L2 129 MB; no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 FLOP x "
-                                    f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz ({peaks['_source']} max clock)",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_source,
                      "kernel": ("transpose_tile_kernel<0> + ffma_tma_kernel, timed together as one sgemm() "
                                 "call; traffic is ffma_tma_kernel's alone"
                                 if kid == sg.KERNEL_FFMA_TMA else sg.KERNEL_NAMES.get(kid, str(kid))),
@@ -492,7 +510,7 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu,
         "parity": parity,
     }
-    if csum and csum.get("sm_mhz"):
+    if csum and csum.get("sm_mhz") and bound == "alu":
         line["roofline"]["frac_at_sampled_clock"] = achieved / acc.ffma_peak_tflops(
             props.multi_processor_count, csum["sm_mhz"])
     if sec is not None:
@@ -517,7 +535,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--tensor-cores", action="store_true",
-                    help="time sgemm_3xtf32 instead of sgemm on the main workload")
+                    help="time sgemm_3xtf32 instead of sgemm on the main workload (= --mode 3xtf32)")
+    ap.add_argument("--mode", choices=sorted(MODES),
+                    help="arithmetic of the main workload: sgemm (fp32), sgemm_3xtf32, sgemm_tf32, "
+                         "sgemm_bf16")
     ap.add_argument("--print-source-hash", metavar="KERNEL")
     args = ap.parse_args()
     if args.print_source_hash:

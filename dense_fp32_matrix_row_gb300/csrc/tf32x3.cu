@@ -36,6 +36,15 @@ namespace {
 
 constexpr int TBM = 128, TBN = 256, TBK = 16;
 constexpr int KC_TILES = 4;                     // k-tiles per accumulation chunk (64 k)
+// One-term kinds: 16 k-tiles (256 k TF32, 512 k BF16).  A chunk of 4 is only
+// 8 MMAs, about as long as the epilogue warps take to drain a 128 x 256
+// accumulator from tensor memory, so the MMAs waited on the drain; measured
+// at 8192^3: 1xTF32 463 -> 557 TFLOP/s, BF16 814 -> 959 TFLOP/s, with the
+// normwise error against the rounded-operand product at 1.5e-8 / 9e-9
+// (4 k-tiles: 1.0e-8 / 7e-9; 64 k-tiles: 4.4e-8 / 4.1e-8).
+#ifndef TF_KC1
+#define TF_KC1 16
+#endif
 constexpr int EPI_WARPS = 8;                    // two warpgroups: 32 rows x 128 columns each
 constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
 constexpr int THREADS = (EPI_WARPS + 2) * 32;
@@ -59,6 +68,8 @@ struct TfCfg {
     static constexpr size_t SMEM = 1024 + (size_t)TSTG * STAGE_BYTES + 256;
     // K elements in one 64-byte row of a tile, and per MMA instruction
     static constexpr int KT = KIND == kTf32 ? TBK : 2 * TBK;
+    // k-tiles per accumulation chunk
+    static constexpr int KC = TERMS == 3 ? KC_TILES : TF_KC1;
     static constexpr int MMA_K = KIND == kTf32 ? 8 : 16;
     static_assert(TERMS == 1 || TERMS == 3, "1xTF32 or 3xTF32");
     static_assert(KIND == kTf32 || TERMS == 1, "BF16 is one term");
@@ -181,7 +192,7 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
     const int tile_n = (pid % per_group) / gsz;
     const int m0 = tile_m * TBM, n0 = tile_n * TBN;
     const int ktiles = (K + KT - 1) / KT;
-    const int nchunks = (ktiles + KC_TILES - 1) / KC_TILES;
+    const int nchunks = (ktiles + L::KC - 1) / L::KC;
     auto stage_ptr = [&](int s, int which) -> uint32_t {   // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
         constexpr int P = L::PARTS;
         const uint32_t off = which < 2 ? which * A_TILE : P * A_TILE + (which - 2) * B_TILE;
@@ -255,8 +266,8 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                     tc_fence_after();
                 }
                 const uint32_t d = tmem + (uint32_t)(b * TBN);
-                const int kt_end = (c + 1) * KC_TILES < ktiles ? (c + 1) * KC_TILES : ktiles;
-                for (int kt = c * KC_TILES; kt < kt_end; ++kt) {
+                const int kt_end = (c + 1) * L::KC < ktiles ? (c + 1) * L::KC : ktiles;
+                for (int kt = c * L::KC; kt < kt_end; ++kt) {
                     const int s = kt % TSTG;
                     if (!mbar_wait(smem_u32(&full[s]), (kt / TSTG) & 1, wait_ns)) {
                         ok = false;
@@ -268,7 +279,7 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                         const uint32_t koff = kk * 32;   // 8 TF32 or 16 BF16 = 32 bytes along K
                         const uint64_t ahi = smem_desc_sw64(stage_ptr(s, 0) + koff);
                         const uint64_t bhi = smem_desc_sw64(stage_ptr(s, 2) + koff);
-                        const uint32_t acc_in = (kt != c * KC_TILES || kk != 0) ? 1u : 0u;
+                        const uint32_t acc_in = (kt != c * L::KC || kk != 0) ? 1u : 0u;
                         if (TERMS == 3) {
                             const uint64_t alo = smem_desc_sw64(stage_ptr(s, 1) + koff);
                             const uint64_t blo = smem_desc_sw64(stage_ptr(s, 3) + koff);
