@@ -16,7 +16,7 @@ import os
 from .build import LIBRARY, build  # noqa: F401  (build is part of the public API)
 
 __all__ = ["sgemm", "sgemm_3xtf32", "sgemm_tf32", "sgemm_bf16", "sgemm_ptr", "status", "select_kernel",
-           "force_kernel", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
+           "force_kernel", "ffma_configs", "ffma_config_for", "ffma_force_config", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
            "version", "SgemmError", "lib"]
 
 OK = 0
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.sgemm_fused.argtypes = _GEMM_ARGS[:-1] + [_vp, ctypes.c_int, ctypes.c_int, _vp]
         L.sgemm_fused.restype = ctypes.c_int
         L.sgemm_select_kernel.argtypes = _GEMM_ARGS[:-1] + [ctypes.c_int]
+        L.sgemm_ffma_config_for.argtypes = [_i64, _i64]
+        L.sgemm_ffma_config_for.restype = ctypes.c_int
         L.sgemm_select_kernel.restype = ctypes.c_int
         L.sgemm_status.argtypes = [_vp]
         L.sgemm_status.restype = ctypes.c_int
@@ -217,6 +219,28 @@ def select_kernel(M, N, K, alpha=1.0, A=16, lda=None, B=16, ldb=None, beta=0.0, 
 
 def force_kernel(kernel_id: int) -> int:
     return int(lib().sgemm_force_kernel(kernel_id))
+
+
+def ffma_configs() -> list[dict]:
+    """The FFMA kernel's compiled tile configurations (index = position)."""
+    out = []
+    for i in range(int(lib().sgemm_ffma_config_count())):
+        v = [ctypes.c_int() for _ in range(6)]
+        if lib().sgemm_ffma_config_info(i, *[ctypes.byref(x) for x in v]) != OK:
+            raise SgemmError(ERR_BAD_ARG, "sgemm_ffma_config_info")
+        out.append(dict(zip(("bm", "bn", "bk", "stages", "threads", "ctas_per_sm"),
+                            (x.value for x in v))))
+    return out
+
+
+def ffma_config_for(M: int, N: int) -> int:
+    """The tile configuration an FFMA-path call of this shape runs."""
+    return int(lib().sgemm_ffma_config_for(int(M), int(N)))
+
+
+def ffma_force_config(idx: int) -> int:
+    """Force FFMA tile configuration ``idx`` (-1: the tuning table); returns the previous."""
+    return int(lib().sgemm_ffma_force_config(int(idx)))
 
 
 def set_wait_limit(ns: int) -> int:

@@ -39,7 +39,8 @@ def sources() -> list[str]:
 
 
 def _inputs() -> list[str]:
-    return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    return (sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.inc"))
+            + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
 def up_to_date() -> bool:

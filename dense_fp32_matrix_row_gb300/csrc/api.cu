@@ -444,6 +444,22 @@ int sgemm_release_workspaces(void) {
     return rc;
 }
 
+int sgemm_ffma_config_count(void) { return ffma_config_count(); }
+
+int sgemm_ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *threads,
+                           int *ctas_per_sm) {
+    if (!bm || !bn || !bk || !stages || !threads || !ctas_per_sm) return SGEMM_ERR_BAD_ARG;
+    return ffma_config_info(idx, bm, bn, bk, stages, threads, ctas_per_sm) ? SGEMM_OK
+                                                                          : SGEMM_ERR_BAD_ARG;
+}
+
+int sgemm_ffma_config_for(int64_t M, int64_t N) { return ffma_config_for(M, N); }
+
+int sgemm_ffma_force_config(int idx) {
+    const int prev = ffma_force_config(idx);
+    return prev == -2 ? SGEMM_ERR_BAD_ARG : prev;
+}
+
 int sgemm_version(void) { return 100; }
 
 }  // extern "C"

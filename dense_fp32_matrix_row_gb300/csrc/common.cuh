@@ -68,6 +68,13 @@ cudaError_t launch_ffma_generic(const GemmArgs &g);
 // partial tiles of the split last wave.
 cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace, int64_t capacity);
 int64_t ffma_tma_workspace_floats(const GemmArgs &g, int64_t capacity);
+// Tile configurations of the FFMA kernel: the one a shape runs (the tuning
+// table, or the forced one), their number, forcing one (-1: the table;
+// returns the previous setting, -2 for a bad index), and their parameters.
+int ffma_config_for(int64_t M, int64_t N);
+int ffma_config_count();
+int ffma_force_config(int idx);
+bool ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *threads, int *minb);
 int64_t ffma_tma_at_ld(int64_t M);
 // Largest M the TMA FFMA kernel's grid can cover.
 int64_t ffma_tma_max_m();

@@ -42,6 +42,12 @@
 #ifndef FFMA_PACKED
 #define FFMA_PACKED 1
 #endif
+#ifndef FFMA_TM
+#define FFMA_TM 8
+#endif
+#ifndef FFMA_TN
+#define FFMA_TN 8
+#endif
 #ifndef FFMA_WM
 #define FFMA_WM 4
 #endif
@@ -79,7 +85,33 @@ struct Cfg {
     static_assert(SMEM * MINB <= 227 * 1024, "shared memory per SM");
 };
 
-using Default = Cfg<8, 8, FFMA_WM, FFMA_WN, FFMA_BK, FFMA_STAGES, FFMA_MINB>;
+// The tile configurations compiled into the library (the search space of the
+// tuning script, dense_fp32_matrix_row_gb300/autotune.py).  Index 0 is the
+// default; ffma_tuning.inc maps shape classes to an index.
+using Default = Cfg<FFMA_TM, FFMA_TN, FFMA_WM, FFMA_WN, FFMA_BK, FFMA_STAGES, FFMA_MINB>;   // 128 x 128
+using Wide = Cfg<8, 8, 2, 4, 32, 2, 2>;                                         // 64 x 256
+using Narrow = Cfg<8, 8, 4, 1, 32, 2, 4>;                                       // 128 x 64
+using ShallowK = Cfg<8, 8, 4, 2, 16, 4, 2>;                                     // 128 x 128, BK 16
+constexpr int kFfmaConfigs = 4;
+
+// f(C{}) for the configuration with index `idx`.
+template <class F>
+decltype(auto) with_config(int idx, F &&f) {
+    switch (idx) {
+        case 1: return f(Wide{});
+        case 2: return f(Narrow{});
+        case 3: return f(ShallowK{});
+        default: return f(Default{});
+    }
+}
+
+struct FfmaTuneEntry {
+    int64_t m_lo, m_max, n_lo, n_max;   // applies to m_lo <= M <= m_max, n_lo <= N <= n_max
+    int config;
+};
+#include "ffma_tuning.inc"
+
+std::atomic<int> g_force_config{-1};
 
 __device__ __forceinline__ float comp(const float4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -426,20 +458,54 @@ int64_t ffma_tma_max_m() { return (int64_t)65535 * Default::BM; }
 
 int64_t ffma_tma_at_ld(int64_t M) { return (M + 3) / 4 * 4; }
 
+int ffma_config_for(int64_t M, int64_t N) {
+    const int forced = g_force_config.load(std::memory_order_relaxed);
+    if (forced >= 0 && forced < kFfmaConfigs) return forced;
+    for (const FfmaTuneEntry &e : kFfmaTune)
+        if (e.m_lo <= M && M <= e.m_max && e.n_lo <= N && N <= e.n_max)
+            return (e.config >= 0 && e.config < kFfmaConfigs) ? e.config : 0;
+    return 0;
+}
+
+int ffma_config_count() { return kFfmaConfigs; }
+
+int ffma_force_config(int idx) {
+    if (idx < -1 || idx >= kFfmaConfigs) return -2;
+    return g_force_config.exchange(idx);
+}
+
+bool ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *threads, int *minb) {
+    if (idx < 0 || idx >= kFfmaConfigs) return false;
+    with_config(idx, [&](auto c) {
+        using C = decltype(c);
+        *bm = C::BM; *bn = C::BN; *bk = C::BK; *stages = C::STAGES; *threads = C::THREADS;
+        *minb = C::MINB;
+        return 0;
+    });
+    return true;
+}
+
 int64_t ffma_tma_workspace_floats(const GemmArgs &g, int64_t capacity) {
     const int64_t at = g.K * ffma_tma_at_ld(g.M);
-    return at + partial_floats<Default>(plan_units<Default>(g, at, capacity));
+    return with_config(ffma_config_for(g.M, g.N), [&](auto c) -> int64_t {
+        using C = decltype(c);
+        return at + partial_floats<C>(plan_units<C>(g, at, capacity));
+    });
 }
 
 cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace, int64_t capacity) {
     const int64_t ldt = ffma_tma_at_ld(g.M);
     const int64_t at = g.K * ldt;
-    const Plan p = plan_units<Default>(g, at, capacity);
-    float *extra = p.parts > 1 ? workspace + at : nullptr;
-    cudaError_t e = launch_transpose(g.M, g.K, g.A, g.lda, workspace, ldt, g.stream,
-                                     reinterpret_cast<unsigned *>(extra), (int)(p.parts > 1 ? p.tail() : 0));
-    if (e != cudaSuccess) return e;
-    return launch_cfg<Default>(g, workspace, ldt, p, extra);
+    return with_config(ffma_config_for(g.M, g.N), [&](auto c) -> cudaError_t {
+        using C = decltype(c);
+        const Plan p = plan_units<C>(g, at, capacity);
+        float *extra = p.parts > 1 ? workspace + at : nullptr;
+        cudaError_t e = launch_transpose(g.M, g.K, g.A, g.lda, workspace, ldt, g.stream,
+                                         reinterpret_cast<unsigned *>(extra),
+                                         (int)(p.parts > 1 ? p.tail() : 0));
+        if (e != cudaSuccess) return e;
+        return launch_cfg<C>(g, workspace, ldt, p, extra);
+    });
 }
 
 }  // namespace sgemm_gb300

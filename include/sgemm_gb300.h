@@ -305,6 +305,31 @@ int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
                   const float *A, int64_t lda, const float *B, int64_t ldb,
                   float beta, float *C, int64_t ldc, void *stream);
 
+/*
+ * FFMA tile configurations (the autotuning of "CUDA 矩阵乘法优化：从朴素 Kernel 到
+ * 接近 cuBLAS", section "8. Kernel 9: 参数自动调优", done per shape class).  The
+ * library holds several compile-time tile configurations of the FFMA kernel;
+ * a table written by dense_fp32_matrix_row_gb300/autotune.py from
+ * measurements picks one per (M, N) class.  These calls serve that script and
+ * the tests; they do not change results beyond rounding order.
+ *   sgemm_ffma_config_count   number of configurations (indices 0 .. n-1;
+ *                             0 is the default)
+ *   sgemm_ffma_config_info    tile rows BM, columns BN, depth BK, pipeline
+ *                             stages, threads per CTA, CTAs per SM the
+ *                             registers are sized for; 0, or SGEMM_ERR_BAD_ARG
+ *                             for an unknown index or a NULL pointer
+ *   sgemm_ffma_config_for     the configuration an FFMA-path call of this M, N
+ *                             runs (host only)
+ *   sgemm_ffma_force_config   make every later FFMA-path call run configuration
+ *                             `idx` (-1: back to the table); returns the
+ *                             previous setting, or SGEMM_ERR_BAD_ARG
+ */
+int sgemm_ffma_config_count(void);
+int sgemm_ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *threads,
+                           int *ctas_per_sm);
+int sgemm_ffma_config_for(int64_t M, int64_t N);
+int sgemm_ffma_force_config(int idx);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int sgemm_version(void);
 

@@ -323,6 +323,26 @@ def test_tf32x3_nan_propagates():
     assert np.isnan(C[7]).all() and np.isfinite(np.delete(C, 7, axis=0)).all()
 
 
+# ---------------------------------------------------------------- FFMA tile configurations
+# Every configuration compiled into the library (the autotuner's choices),
+# forced, on shapes with ragged edges, a split last wave and beta != 0.
+@pytest.mark.parametrize("cfg", range(4))
+@pytest.mark.parametrize("M,N,K", [(300, 260, 516), (1500, 1100, 700), (129, 1000, 77),
+                                   (2300, 2352, 1001)])
+def test_every_ffma_config(cfg, M, N, K):
+    assert len(sg.ffma_configs()) == 4
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=M + cfg, beta=0.5)
+    ldb = (N + 3) // 4 * 4
+    prev = sg.ffma_force_config(cfg)
+    try:
+        _, chosen = run_checked(sg, A, B, C0, 1.5, 0.5, lds=(K, ldb, N + 1))
+        assert chosen == TMA
+        Ai, Bi, Ci = make_inputs(M, N, min(K, 300), "int", seed=cfg, beta=-1.0)
+        run_checked(sg, Ai, Bi, Ci, 2.0, -1.0, exact=True, lds=(min(K, 300), ldb, N))
+    finally:
+        sg.ffma_force_config(prev)
+
+
 # ---------------------------------------------------------------- fused epilogue
 # C = act(alpha*A@B + beta*C + bias[j]) on every kernel path: the TMA tile
 # kernel (whole tiles and a split last wave), the plain-load kernel, the three
