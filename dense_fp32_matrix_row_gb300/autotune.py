@@ -212,7 +212,9 @@ print("RESULT", json.dumps({{f"{{M}}x{{N}}x{{K}}": autotune._time(sg, torch, M, 
 
 
 def run_search(workdir: str, shapes: list[tuple[int, int, int]], tiles) -> None:
-    from . import build as b
+    # the package re-exports the build() function under the module's name,
+    # so import the function itself
+    from .build import build as build_library
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     results = {}
     for cand in candidates(tiles):
@@ -220,7 +222,7 @@ def run_search(workdir: str, shapes: list[tuple[int, int, int]], tiles) -> None:
         flags = [f"-DFFMA_{k}={v}" for k, v in zip(("TM", "TN", "WM", "WN", "BK", "STAGES", "MINB"), cand)]
         lib = os.path.join(workdir, name, "libsgemm_gb300.so")
         try:
-            b.build(extra_flags=flags, library=lib)
+            build_library(extra_flags=flags, library=lib)
         except Exception as e:  # a combination ptxas rejects
             print(name, "build failed:", str(e)[-200:], flush=True)
             continue
@@ -232,6 +234,8 @@ def run_search(workdir: str, shapes: list[tuple[int, int, int]], tiles) -> None:
             continue
         results[name] = json.loads(line[0][7:])
         print(name, results[name], flush=True)
+    if not results:
+        raise RuntimeError("no configuration built and ran")
     best = max(results.items(), key=lambda kv: sum(kv[1].values()))
     print("best", best[0], best[1])
 
