@@ -15,7 +15,7 @@ import os
 
 from .build import LIBRARY, build  # noqa: F401  (build is part of the public API)
 
-__all__ = ["sgemm", "sgemm_3xtf32", "sgemm_tf32", "sgemm_bf16", "sgemm_ptr", "status", "select_kernel",
+__all__ = ["sgemm", "sgemm_host", "host_set_panels", "host_panel_rows", "sgemm_3xtf32", "sgemm_tf32", "sgemm_bf16", "sgemm_ptr", "status", "select_kernel",
            "force_kernel", "ffma_configs", "ffma_config_for", "ffma_force_config", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
            "version", "SgemmError", "lib"]
 
@@ -74,6 +74,12 @@ def lib() -> ctypes.CDLL:
             getattr(L, name).restype = ctypes.c_int
         L.sgemm_fused.argtypes = _GEMM_ARGS[:-1] + [_vp, ctypes.c_int, ctypes.c_int, _vp]
         L.sgemm_fused.restype = ctypes.c_int
+        L.sgemm_host.argtypes = _GEMM_ARGS[:-1] + [ctypes.c_int, _vp]
+        L.sgemm_host.restype = ctypes.c_int
+        L.sgemm_host_set_panels.argtypes = [ctypes.c_int]
+        L.sgemm_host_set_panels.restype = ctypes.c_int
+        L.sgemm_host_panel_rows.argtypes = [_i64, _i64, _i64]
+        L.sgemm_host_panel_rows.restype = _i64
         L.sgemm_select_kernel.argtypes = _GEMM_ARGS[:-1] + [ctypes.c_int]
         L.sgemm_ffma_config_for.argtypes = [_i64, _i64]
         L.sgemm_ffma_config_for.restype = ctypes.c_int
@@ -183,6 +189,47 @@ def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
                                _stream_handle(stream, dev)))
     if rc != OK:
         raise SgemmError(rc, "sgemm_fused")
+
+
+def sgemm_host(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None,
+               tensor_cores=False) -> None:
+    """C <- alpha * A @ B + beta * C on torch CPU float32 tensors (pinned
+    memory lets the copies overlap the compute), through the C ABI's
+    sgemm_host: the library copies B and row panels of A and C to the device,
+    multiplies each panel as it arrives and copies its rows of C back.
+    Enqueued on ``stream`` (default: the current torch stream); C holds the
+    result once that stream is synchronised.  ``tensor_cores`` selects the
+    arithmetic as in ``sgemm``.  Raises SgemmError on a rejected call."""
+    import torch
+    for t, n in ((A, "A"), (B, "B"), (C, "C")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or t.dim() != 2:
+            raise TypeError(f"{n} must be a 2-D float32 tensor")
+        if t.is_cuda:
+            raise TypeError(f"{n} must live in host memory (use sgemm for device tensors)")
+        if t.shape[1] > 1 and t.stride(1) != 1 and t.numel():
+            raise ValueError(f"{n} must be row-major with contiguous rows (stride(1) == 1)")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    rc = int(lib().sgemm_host(M, N, K, float(alpha), A.data_ptr() or None, _ld(A),
+                              B.data_ptr() or None, _ld(B), float(beta), C.data_ptr() or None,
+                              _ld(C), _mode(tensor_cores), _stream_handle(stream)))
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_host")
+
+
+def host_set_panels(panels: int) -> int:
+    """Force sgemm_host's panel count (0: the library's choice); returns the previous setting."""
+    rc = int(lib().sgemm_host_set_panels(int(panels)))
+    if rc < 0:
+        raise SgemmError(rc, "sgemm_host_set_panels")
+    return rc
+
+
+def host_panel_rows(M: int, N: int, K: int) -> int:
+    """Rows per panel that sgemm_host would use for this shape."""
+    return int(lib().sgemm_host_panel_rows(M, N, K))
 
 
 def sgemm_3xtf32(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None) -> None:

@@ -428,8 +428,8 @@ int sgemm_selftest_wait(int64_t ns, void *stream) {
 }
 
 int sgemm_release_workspaces(void) {
+    int rc = release_host_paths() ? SGEMM_OK : SGEMM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_ws_mu);
-    int rc = SGEMM_OK;
     int cur = 0;
     if (cudaGetDevice(&cur) != cudaSuccess) return SGEMM_ERR_CUDA;
     for (auto &kv : g_ws) {

@@ -109,6 +109,9 @@ cudaError_t launch_selftest_wait(unsigned *err, uint64_t wait_ns, cudaStream_t s
 cudaError_t launch_tf32(const GemmArgs &g, float *workspace, int terms);
 size_t tf32_workspace_floats(int64_t M, int64_t N, int64_t K, int terms);
 bool tf32x3_can_run(int64_t M, int64_t N, int64_t K);
+// Frees the buffers, streams and events of sgemm_host's pipelines (after
+// waiting for them); false if a CUDA call failed.
+bool release_host_paths();
 // Fills g.err, g.wait_ns, g.sm_count and g.encode for the current device
 // (setting the device up on first use); returns an SGEMM_* status.
 int fill_device_args(GemmArgs &g);

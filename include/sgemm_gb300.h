@@ -259,12 +259,59 @@ int64_t sgemm_set_wait_limit(int64_t ns);
 int sgemm_selftest_wait(int64_t ns, void *stream);
 
 /*
+ * sgemm_host -- the product of sgemm_fused(..., bias = NULL, SGEMM_ACT_NONE,
+ * mode, stream) for operands that live in HOST memory.
+ *
+ * The pages overlap loading with computing between global and shared memory
+ * ("GPU GEMM 优化完全拆解（一）", section "分块的思想：把 K 循环切成一段段":
+ * double buffering and asynchronous copies hide the loads behind the
+ * arithmetic) and queue work asynchronously from the host ("GPU 基础原理",
+ * section "3. 第三种区间：开销").  This entry point applies the same overlap one
+ * level up, between host and device memory: B is copied to the device, then
+ * A and C (C only when beta != 0) follow in row panels on a copy stream;
+ * each panel is multiplied on `stream` as soon as it has arrived, and its
+ * rows of C go back to the host on a second copy stream while the next
+ * panel is multiplied.  Two device slots hold consecutive panels.
+ *   A, B, C     HOST pointers (device pointers also work: the copies use
+ *               cudaMemcpyDefault), row-major with lda, ldb, ldc as in
+ *               sgemm().  Page-locked (pinned) host memory lets the copies
+ *               run asynchronously and overlap; pageable memory works, but
+ *               the driver then stages every copy and the call returns only
+ *               once the copies back have finished.
+ *   mode        SGEMM_MODE_*: the arithmetic and kernels of sgemm(),
+ *               sgemm_3xtf32(), sgemm_tf32() or sgemm_bf16() (each panel is
+ *               one call of that entry point, so results match it up to the
+ *               kernel choice for the panel's row count).
+ *   stream      the call is ordered after earlier work on `stream` and
+ *               completes before later work on it: C holds the result once
+ *               the stream is synchronised (cudaStreamSynchronize, or
+ *               sgemm_status(stream)).  A, B and C must stay valid and C
+ *               untouched until then.
+ * Memory: the library keeps one device buffer per (device, stream) holding
+ * B and two panels of A and C (grown with cudaMallocAsync on `stream`; freed
+ * by sgemm_release_workspaces), plus two copy streams and a few events.
+ * Panel rows: a multiple of 128 chosen so each panel still fills the GPU
+ * (sgemm_host_panel_rows reports it; sgemm_host_set_panels overrides the
+ * panel count, 0 restores the library's choice and the previous setting is
+ * returned).  Products with M <= 256 or without an A@B term run as one panel.
+ * Errors: those of sgemm(); SGEMM_ERR_CAPTURE while `stream` is being
+ * captured (the call is not capturable).  An error after some work was
+ * enqueued still leaves `stream` ordered after that work.
+ */
+int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha,
+               const float *A, int64_t lda, const float *B, int64_t ldb,
+               float beta, float *C, int64_t ldc, int mode, void *stream);
+int sgemm_host_set_panels(int panels);
+int64_t sgemm_host_panel_rows(int64_t M, int64_t N, int64_t K);
+
+/*
  * sgemm_release_workspaces -- free the library's cached device workspaces
  * (the transposed copy of A that the FFMA kernel stages from; one buffer per
- * device and stream, grown with cudaMallocAsync on the call's stream).
- * Waits for every stream that owns a workspace.  Safe to call at any time
- * from a thread that has no sgemm call in progress; later calls allocate
- * again as needed.  Returns SGEMM_OK or SGEMM_ERR_CUDA.
+ * device and stream, grown with cudaMallocAsync on the call's stream) and
+ * sgemm_host's device buffers, copy streams and events.
+ * Waits for every stream that owns a workspace.  Call it only while no other
+ * host thread is inside an sgemm call; later calls allocate again as needed.
+ * Returns SGEMM_OK or SGEMM_ERR_CUDA.
  */
 int sgemm_release_workspaces(void);
 

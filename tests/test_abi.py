@@ -139,3 +139,47 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sg, "LIBRARY", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="not built"):
         sg.lib()
+
+
+def host_call(L, M, N, K, A=1 << 20, lda=None, B=1 << 26, ldb=None, C=1 << 32, ldc=None,
+              mode=0, alpha=1.0, beta=0.0):
+    return int(L.sgemm_host(M, N, K, alpha, A, K if lda is None else lda, B,
+                            N if ldb is None else ldb, beta, C, N if ldc is None else ldc, mode,
+                            None))
+
+
+def test_host_path_argument_errors(L):
+    # rejected on the host before any CUDA call (none would succeed here)
+    assert host_call(L, -1, 4, 4) == sg.ERR_BAD_DIM
+    assert host_call(L, 4, 4, 4, lda=3) == sg.ERR_BAD_LD
+    assert host_call(L, 4, 4, 4, ldc=3) == sg.ERR_BAD_LD
+    assert host_call(L, 4, 4, 4, C=0) == sg.ERR_NULL_PTR
+    assert host_call(L, 64, 64, 64, A=1 << 20, C=(1 << 20) + 400) == sg.ERR_ALIAS
+    assert host_call(L, 4, 4, 4, mode=9) == sg.ERR_BAD_ARG
+    assert host_call(L, 0, 4, 4) == sg.OK   # nothing to do
+    assert L.sgemm_host_set_panels(-1) == sg.ERR_BAD_ARG
+
+
+def test_host_path_panels(L):
+    prev = sg.host_set_panels(0)
+    try:
+        # skinny products and products without A@B: one panel
+        assert sg.host_panel_rows(16, 14336, 4096) == 16
+        assert sg.host_panel_rows(256, 4096, 4096) == 256
+        assert sg.host_panel_rows(5000, 4096, 0) == 5000
+        assert sg.host_panel_rows(0, 5, 5) == 0
+        assert sg.host_panel_rows(-1, 5, 5) == sg.ERR_BAD_DIM
+        for M, N in ((4092, 4092), (8192, 8192), (8192, 14336), (1000, 300), (300, 20000)):
+            r = sg.host_panel_rows(M, N, 4096)
+            assert 1 <= r <= M
+            assert r == M or r % 128 == 0
+            assert -(-M // r) <= 8
+        # forced counts: rows rounded up to 128, never more panels than asked
+        for P in (1, 2, 3, 5, 8):
+            sg.host_set_panels(P)
+            r = sg.host_panel_rows(4092, 4092, 4092)
+            assert r == (4092 if P == 1 else min(4092, -(-(-(-4092 // P)) // 128) * 128))
+            assert -(-4092 // r) <= P
+        assert sg.host_set_panels(0) == 8
+    finally:
+        sg.host_set_panels(prev)
