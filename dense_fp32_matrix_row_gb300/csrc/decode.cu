@@ -439,7 +439,10 @@ __device__ __forceinline__ void fma_row8(float (&acc)[8], float a, const float (
 //
 // After the K loop the k groups' partial tiles are summed in a fixed order
 // in shared memory, then across the cluster.
-constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32, DO_TKB = 16;
+#ifndef DECODE_DO_TKB
+#define DECODE_DO_TKB 16   // k-steps per TMA stage
+#endif
+constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32, DO_TKB = DECODE_DO_TKB;
 #ifndef DECODE_DO_STAGES
 #define DECODE_DO_STAGES 2
 #endif

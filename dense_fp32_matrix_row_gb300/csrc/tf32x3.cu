@@ -34,8 +34,8 @@
 namespace sgemm_gb300 {
 namespace {
 
-constexpr int TBM = 128, TBN = 256, TBK = 16;
-constexpr int KC_TILES = 4;                     // k-tiles per accumulation chunk (64 k)
+constexpr int TBM = 128, TBN = 256;
+constexpr int KC_TILES = 4;                     // 3xTF32: k-tiles per accumulation chunk (64 k)
 // One-term kinds: 16 k-tiles (256 k TF32, 512 k BF16).  A chunk of 4 is only
 // 8 MMAs, about as long as the epilogue warps take to drain a 128 x 256
 // accumulator from tensor memory, so the MMAs waited on the drain; measured
@@ -43,19 +43,25 @@ constexpr int KC_TILES = 4;                     // k-tiles per accumulation chun
 // normwise error against the rounded-operand product at 1.5e-8 / 9e-9
 // (4 k-tiles: 1.0e-8 / 7e-9; 64 k-tiles: 4.4e-8 / 4.1e-8).
 #ifndef TF_KC1
-#define TF_KC1 16
+#define TF_KC1 16   // in 64-byte k-tiles; scaled to the row width actually used
+#endif
+// Swizzle span (= bytes of K per operand row of a stage) of the one-term
+// kinds.  128-byte rows move each stage in half as many TMA requests as
+// 64-byte rows; the one-term kinds are bound by operand delivery, the
+// 3-term kind by the tensor pipe, so only the former use them.
+#ifndef TF_SW1
+#define TF_SW1 128
 #endif
 constexpr int EPI_WARPS = 8;                    // two warpgroups: 32 rows x 128 columns each
 constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
 constexpr int THREADS = (EPI_WARPS + 2) * 32;
 constexpr int EPI_COLS = TBN / (EPI_WARPS / 4); // columns per epilogue thread
 constexpr int RASTER_GROUP = 16;                // M tiles walked together (L2 reuse)
-constexpr uint32_t A_TILE = TBM * TBK * 4;                 // 8 KB
-constexpr uint32_t B_TILE = TBN * TBK * 4;                 // 16 KB
 constexpr uint32_t TMEM_COLS = 2 * TBN;                    // two 128 x 256 FP32 accumulators
 
-// Per-stage layout: the A parts, then the B parts (hi, then lo for 3 terms).
-// 3 terms: 48 KB stages, 4 deep; 1 term: 24 KB stages, 8 deep (192 KB both).
+// Per-stage layout: the A parts, then the B parts (hi, then lo for 3 terms),
+// each tile rows x SWB bytes of K.  3 terms (64-byte rows): 48 KB stages, 4
+// deep; 1 term (128-byte rows): 48 KB stages, 4 deep (192 KB both).
 // Operand kinds: FP32 bit patterns read as TF32 (kind::tf32), or BF16
 // (kind::f16 with both operands BF16).
 enum : int { kTf32 = 0, kBf16 = 1 };
@@ -63,22 +69,24 @@ enum : int { kTf32 = 0, kBf16 = 1 };
 template <int TERMS, int KIND = kTf32>
 struct TfCfg {
     static constexpr int PARTS = TERMS == 3 ? 2 : 1;
+    static constexpr int SWB = TERMS == 3 ? 64 : TF_SW1;          // bytes of K per tile row
+    static constexpr uint32_t A_TILE = TBM * SWB, B_TILE = TBN * SWB;
     static constexpr uint32_t STAGE_BYTES = PARTS * (A_TILE + B_TILE);
-    static constexpr int TSTG = TERMS == 3 ? 4 : 8;
+    static constexpr int TSTG = (192 * 1024) / STAGE_BYTES;
     static constexpr size_t SMEM = 1024 + (size_t)TSTG * STAGE_BYTES + 256;
-    // K elements in one 64-byte row of a tile, and per MMA instruction
-    static constexpr int KT = KIND == kTf32 ? TBK : 2 * TBK;
-    // k-tiles per accumulation chunk
-    static constexpr int KC = TERMS == 3 ? KC_TILES : TF_KC1;
+    // K elements in one row of a tile, and per MMA instruction (32 bytes)
+    static constexpr int KT = KIND == kTf32 ? SWB / 4 : SWB / 2;
     static constexpr int MMA_K = KIND == kTf32 ? 8 : 16;
+    // k-tiles per accumulation chunk: 64 k (3 terms), TF_KC1 64-byte k-tiles (1 term)
+    static constexpr int KC = TERMS == 3 ? KC_TILES : TF_KC1 * 64 / SWB;
+    static_assert(SWB == 64 || SWB == 128, "64- or 128-byte swizzle");
+    static_assert(A_TILE % 1024 == 0 && B_TILE % 1024 == 0, "tiles keep 1024-byte alignment");
+    static_assert(KC >= 1 && TSTG >= 2, "chunk and ring depth");
     static_assert(TERMS == 1 || TERMS == 3, "1xTF32 or 3xTF32");
     static_assert(KIND == kTf32 || TERMS == 1, "BF16 is one term");
     static_assert(SMEM <= 227 * 1024, "shared memory per block");
-    static_assert(KT / MMA_K == 2, "two MMAs of 32 bytes of K per 64-byte row");
 };
 constexpr uint64_t DRAIN_NS = 1000000000ull;
-static_assert(TBK * 4 == 64, "rows of a K slice fill exactly one 64-byte swizzle span");
-static_assert(A_TILE % 1024 == 0 && B_TILE % 1024 == 0, "tiles keep 1024-byte alignment");
 static_assert(EPI_WARPS % 4 == 0 && EPI_COLS % 16 == 0, "epilogue covers all lanes and columns");
 
 // Instruction descriptor of tcgen05.mma kind::tf32: D format F32 (bits 4-5 = 1),
@@ -93,15 +101,19 @@ constexpr uint32_t IDESC_BF16 = (1u << 4) | (BF16_FORMAT << 7) | (BF16_FORMAT <<
                                 ((uint32_t)(TBN >> 3) << 17) | ((uint32_t)(TBM >> 4) << 24);
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
-// with the 64-byte swizzle: rows of 64 bytes, 8-row core groups 512 bytes
-// apart (stride byte offset), descriptor version 1, layout SWIZZLE_64B (4).
-__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr) {
+// with the SWB-byte swizzle: rows of SWB bytes, 8-row core groups 8*SWB
+// bytes apart (stride byte offset), descriptor version 1, layout
+// SWIZZLE_64B (4) or SWIZZLE_128B (2).  A k-offset inside the row is added
+// to the start address; the swizzle is a function of the address bits.
+template <int SWB>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    static_assert(SWB == 64 || SWB == 128, "64- or 128-byte swizzle");
     uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);           // start address
-    d |= (uint64_t)1 << 16;                            // leading byte offset (unused here)
-    d |= (uint64_t)((512u >> 4) & 0x3FFFu) << 32;      // stride byte offset
-    d |= (uint64_t)1 << 46;                            // version
-    d |= (uint64_t)4 << 61;                            // SWIZZLE_64B
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);               // start address
+    d |= (uint64_t)1 << 16;                                // leading byte offset (unused here)
+    d |= (uint64_t)(((8u * SWB) >> 4) & 0x3FFFu) << 32;    // stride byte offset
+    d |= (uint64_t)1 << 46;                                // version
+    d |= (uint64_t)(SWB == 128 ? 2 : 4) << 61;             // layout
     return d;
 }
 
@@ -195,7 +207,8 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
     const int nchunks = (ktiles + L::KC - 1) / L::KC;
     auto stage_ptr = [&](int s, int which) -> uint32_t {   // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
         constexpr int P = L::PARTS;
-        const uint32_t off = which < 2 ? which * A_TILE : P * A_TILE + (which - 2) * B_TILE;
+        const uint32_t off =
+            which < 2 ? which * L::A_TILE : P * L::A_TILE + (which - 2) * L::B_TILE;
         return smem_u32(ring + (size_t)s * STAGE_BYTES + off);
     };
 
@@ -277,12 +290,12 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
 #pragma unroll
                     for (int kk = 0; kk < KT / L::MMA_K; ++kk) {
                         const uint32_t koff = kk * 32;   // 8 TF32 or 16 BF16 = 32 bytes along K
-                        const uint64_t ahi = smem_desc_sw64(stage_ptr(s, 0) + koff);
-                        const uint64_t bhi = smem_desc_sw64(stage_ptr(s, 2) + koff);
+                        const uint64_t ahi = smem_desc<L::SWB>(stage_ptr(s, 0) + koff);
+                        const uint64_t bhi = smem_desc<L::SWB>(stage_ptr(s, 2) + koff);
                         const uint32_t acc_in = (kt != c * L::KC || kk != 0) ? 1u : 0u;
                         if (TERMS == 3) {
-                            const uint64_t alo = smem_desc_sw64(stage_ptr(s, 1) + koff);
-                            const uint64_t blo = smem_desc_sw64(stage_ptr(s, 3) + koff);
+                            const uint64_t alo = smem_desc<L::SWB>(stage_ptr(s, 1) + koff);
+                            const uint64_t blo = smem_desc<L::SWB>(stage_ptr(s, 3) + koff);
                             tc_mma_tf32(d, ahi, blo, acc_in);
                             tc_mma_tf32(d, alo, bhi, 1u);
                             tc_mma_tf32(d, ahi, bhi, 1u);
@@ -431,13 +444,14 @@ cudaError_t launch_terms(const GemmArgs &g, float *ws) {
     if (e != cudaSuccess) return e;
 
     alignas(64) CUtensorMap tAhi, tAlo, tBhi, tBlo;
-    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!encode_tma_2d(g.encode, &tAhi, ahi, g.K, g.M, ldk, TBK, TBM, sw) ||
-        !encode_tma_2d(g.encode, &tBhi, bhi, g.K, g.N, ldk, TBK, TBN, sw))
+    const CUtensorMapSwizzle sw = L::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    constexpr uint32_t kt = L::KT;
+    if (!encode_tma_2d(g.encode, &tAhi, ahi, g.K, g.M, ldk, kt, TBM, sw) ||
+        !encode_tma_2d(g.encode, &tBhi, bhi, g.K, g.N, ldk, kt, TBN, sw))
         return cudaErrorInvalidValue;
     if (TERMS == 3) {
-        if (!encode_tma_2d(g.encode, &tAlo, alo, g.K, g.M, ldk, TBK, TBM, sw) ||
-            !encode_tma_2d(g.encode, &tBlo, blo, g.K, g.N, ldk, TBK, TBN, sw))
+        if (!encode_tma_2d(g.encode, &tAlo, alo, g.K, g.M, ldk, kt, TBM, sw) ||
+            !encode_tma_2d(g.encode, &tBlo, blo, g.K, g.N, ldk, kt, TBN, sw))
             return cudaErrorInvalidValue;
     } else {
         tAlo = tAhi;   // never read
@@ -450,15 +464,16 @@ cudaError_t launch_terms(const GemmArgs &g, float *ws) {
 // 16-bit arrays, ldk = K rounded up to 8 (16-byte rows).
 cudaError_t launch_bf16_terms(const GemmArgs &g, float *ws) {
     const int64_t ldk = bf16_ld(g.K);
-    const int64_t asz = (g.M * ldk + 127) / 128 * 128, bsz = (g.N * ldk + 127) / 128 * 128;
+    const int64_t asz = (g.M * ldk + 127) / 128 * 128;
     __nv_bfloat16 *a = reinterpret_cast<__nv_bfloat16 *>(ws), *b = a + asz;
     cudaError_t e = launch_bf16_rows(g.M, g.K, g.A, g.lda, a, ldk, g.stream);
     if (e != cudaSuccess) return e;
     e = launch_bf16_transpose(g.K, g.N, g.B, g.ldb, b, ldk, g.stream);
     if (e != cudaSuccess) return e;
     alignas(64) CUtensorMap tA, tB;
-    const CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_64B;
-    constexpr uint32_t kt = TfCfg<1, kBf16>::KT;
+    using L = TfCfg<1, kBf16>;
+    const CUtensorMapSwizzle sw = L::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    constexpr uint32_t kt = L::KT;
     if (!encode_tma_2d_bf16(g.encode, &tA, a, g.K, g.M, ldk, kt, TBM, sw) ||
         !encode_tma_2d_bf16(g.encode, &tB, b, g.K, g.N, ldk, kt, TBN, sw))
         return cudaErrorInvalidValue;
