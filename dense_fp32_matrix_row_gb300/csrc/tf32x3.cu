@@ -16,7 +16,8 @@
 //     K-major -- the canonical UMMA layout;
 //  2. the MMA kernel: one CTA per 128 x 256 tile of C.  Warp 8 streams 16-wide
 //     K slices of the four operand tiles into a 4-stage shared-memory ring
-//     with TMA (64-byte swizzle); one thread of warp 9 issues, per 8-wide k
+//     with TMA (64-byte swizzle; the one-term kinds below stream 128-byte K
+//     rows with the 128-byte swizzle); one thread of warp 9 issues, per 8-wide k
 //     step, three tcgen05.mma kind::tf32 (hi*lo, lo*hi, hi*hi) into one FP32
 //     accumulator of 128 lanes x 256 columns in tensor memory and releases
 //     each stage with tcgen05.commit; warps 0-7 read the accumulator back with
@@ -52,6 +53,9 @@ constexpr int KC_TILES = 4;                     // 3xTF32: k-tiles per accumulat
 #ifndef TF_SW1
 #define TF_SW1 128
 #endif
+#ifndef TF_SW3
+#define TF_SW3 64   // measured at 8192^3: 128-byte rows (two 96 KB stages) 271 vs 297 TFLOP/s
+#endif
 constexpr int EPI_WARPS = 8;                    // two warpgroups: 32 rows x 128 columns each
 constexpr int PRODUCER_WARP = EPI_WARPS, MMA_WARP = EPI_WARPS + 1;
 constexpr int THREADS = (EPI_WARPS + 2) * 32;
@@ -69,7 +73,7 @@ enum : int { kTf32 = 0, kBf16 = 1 };
 template <int TERMS, int KIND = kTf32>
 struct TfCfg {
     static constexpr int PARTS = TERMS == 3 ? 2 : 1;
-    static constexpr int SWB = TERMS == 3 ? 64 : TF_SW1;          // bytes of K per tile row
+    static constexpr int SWB = TERMS == 3 ? TF_SW3 : TF_SW1;      // bytes of K per tile row
     static constexpr uint32_t A_TILE = TBM * SWB, B_TILE = TBN * SWB;
     static constexpr uint32_t STAGE_BYTES = PARTS * (A_TILE + B_TILE);
     static constexpr int TSTG = (192 * 1024) / STAGE_BYTES;
