@@ -37,14 +37,15 @@ namespace {
 
 constexpr int TBM = 128, TBN = 256;
 constexpr int KC_TILES = 4;                     // 3xTF32: k-tiles per accumulation chunk (64 k)
-// One-term kinds: 16 k-tiles (256 k TF32, 512 k BF16).  A chunk of 4 is only
-// 8 MMAs, about as long as the epilogue warps take to drain a 128 x 256
-// accumulator from tensor memory, so the MMAs waited on the drain; measured
-// at 8192^3: 1xTF32 463 -> 557 TFLOP/s, BF16 814 -> 959 TFLOP/s, with the
-// normwise error against the rounded-operand product at 1.5e-8 / 9e-9
-// (4 k-tiles: 1.0e-8 / 7e-9; 64 k-tiles: 4.4e-8 / 4.1e-8).
+// One-term kinds: 512 k (TF32) / 1024 k (BF16) per chunk.  A 64 k chunk is
+// only 8 MMAs, about as long as the epilogue warps take to drain a 128 x 256
+// accumulator from tensor memory, so the MMAs waited on the drain.  Measured
+// at 8192^3 (TFLOP/s / normwise error against the rounded-operand product,
+// TF32 and BF16): 64 k 463 / 1.0e-8 and 814 / 7e-9; 256 k 557 / 1.5e-8 and
+// 959 / 9e-9 (64-byte rows, one CTA per tile); in the persistent kernel with
+// 128-byte rows 256 k 718 and 1240, 512 k 741 / 2.4e-8 and 1282 / 1.7e-8.
 #ifndef TF_KC1
-#define TF_KC1 16   // in 64-byte k-tiles; scaled to the row width actually used
+#define TF_KC1 32   // in 64-byte k-tiles (512 k TF32, 1024 k BF16); scaled to the row width used
 #endif
 // Swizzle span (= bytes of K per operand row of a stage) of the one-term
 // kinds.  128-byte rows move each stage in half as many TMA requests as
@@ -52,6 +53,9 @@ constexpr int KC_TILES = 4;                     // 3xTF32: k-tiles per accumulat
 // 3-term kind by the tensor pipe, so only the former use them.
 #ifndef TF_SW1
 #define TF_SW1 128
+#endif
+#ifndef TF_PERSIST
+#define TF_PERSIST 1
 #endif
 #ifndef TF_SW3
 #define TF_SW3 64   // measured at 8192^3: 128-byte rows (two 96 KB stages) 271 vs 297 TFLOP/s
@@ -197,16 +201,18 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drainbar + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Grouped rasterisation: RASTER_GROUP M-tiles x all N-tiles per group, so
-    // the blocks resident at one time share a few A and B panels through L2.
+    // Persistent: CTA b takes tiles b, b + gridDim.x, ...  Grouped
+    // rasterisation: RASTER_GROUP M-tiles x all N-tiles per group, so the
+    // tiles in flight at one time share a few A and B panels through L2.
     const int num_m = (M + TBM - 1) / TBM, num_n = (N + TBN - 1) / TBN;
-    const int pid = blockIdx.x;
+    const int tiles = num_m * num_n;
     const int per_group = RASTER_GROUP * num_n;
-    const int first_m = (pid / per_group) * RASTER_GROUP;
-    const int gsz = (num_m - first_m) < RASTER_GROUP ? (num_m - first_m) : RASTER_GROUP;
-    const int tile_m = first_m + (pid % per_group) % gsz;
-    const int tile_n = (pid % per_group) / gsz;
-    const int m0 = tile_m * TBM, n0 = tile_n * TBN;
+    auto tile_origin = [&](int t, int &m0, int &n0) {
+        const int first_m = (t / per_group) * RASTER_GROUP;
+        const int gsz = (num_m - first_m) < RASTER_GROUP ? (num_m - first_m) : RASTER_GROUP;
+        m0 = (first_m + (t % per_group) % gsz) * TBM;
+        n0 = ((t % per_group) / gsz) * TBN;
+    };
     const int ktiles = (K + KT - 1) / KT;
     const int nchunks = (ktiles + L::KC - 1) / L::KC;
     auto stage_ptr = [&](int s, int which) -> uint32_t {   // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
@@ -249,23 +255,32 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                 tma_prefetch_desc(&tmAlo);
                 tma_prefetch_desc(&tmBlo);
             }
-            int kt = 0;
-            for (; kt < ktiles; ++kt) {
-                const int s = kt % TSTG;
-                const uint32_t use = kt / TSTG;
-                if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, wait_ns)) break;
-                const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                tma_load_2d(stage_ptr(s, 0), &tmAhi, fb, kt * KT, m0);
-                tma_load_2d(stage_ptr(s, 2), &tmBhi, fb, kt * KT, n0);
-                if (TERMS == 3) {
-                    tma_load_2d(stage_ptr(s, 1), &tmAlo, fb, kt * KT, m0);
-                    tma_load_2d(stage_ptr(s, 3), &tmBlo, fb, kt * KT, n0);
+            uint32_t g = 0;   // k-tiles issued by this CTA, over all its tiles
+            bool ok = true;
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                int m0, n0;
+                tile_origin(t, m0, n0);
+                for (int kt = 0; kt < ktiles; ++kt) {
+                    const int s = (int)(g % TSTG);
+                    const uint32_t use = g / TSTG;
+                    if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    tma_load_2d(stage_ptr(s, 0), &tmAhi, fb, kt * KT, m0);
+                    tma_load_2d(stage_ptr(s, 2), &tmBhi, fb, kt * KT, n0);
+                    if (TERMS == 3) {
+                        tma_load_2d(stage_ptr(s, 1), &tmAlo, fb, kt * KT, m0);
+                        tma_load_2d(stage_ptr(s, 3), &tmBlo, fb, kt * KT, n0);
+                    }
+                    ++g;
                 }
             }
-            if (kt < ktiles) {
+            if (!ok) {
                 record_error(err, kErrWaitTimeout);
-                for (int q = (kt > TSTG ? kt - TSTG : 0); q < kt; ++q)
+                for (uint32_t q = (g > TSTG ? g - TSTG : 0); q < g; ++q)
                     mbar_wait(smem_u32(&full[q % TSTG]), (q / TSTG) & 1, DRAIN_NS);
             }
         }
@@ -273,46 +288,51 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
         if (lane == 0) {
             bool ok = true;
             bool issued_any = false;
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const int b = c & 1;
-                if (c >= 2) {   // the epilogue must have read this buffer's previous chunk
-                    if (!mbar_wait(smem_u32(&cempty[b]), ((c >> 1) - 1) & 1, wait_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
-                const uint32_t d = tmem + (uint32_t)(b * TBN);
-                const int kt_end = (c + 1) * L::KC < ktiles ? (c + 1) * L::KC : ktiles;
-                for (int kt = c * L::KC; kt < kt_end; ++kt) {
-                    const int s = kt % TSTG;
-                    if (!mbar_wait(smem_u32(&full[s]), (kt / TSTG) & 1, wait_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < KT / L::MMA_K; ++kk) {
-                        const uint32_t koff = kk * 32;   // 8 TF32 or 16 BF16 = 32 bytes along K
-                        const uint64_t ahi = smem_desc<L::SWB>(stage_ptr(s, 0) + koff);
-                        const uint64_t bhi = smem_desc<L::SWB>(stage_ptr(s, 2) + koff);
-                        const uint32_t acc_in = (kt != c * L::KC || kk != 0) ? 1u : 0u;
-                        if (TERMS == 3) {
-                            const uint64_t alo = smem_desc<L::SWB>(stage_ptr(s, 1) + koff);
-                            const uint64_t blo = smem_desc<L::SWB>(stage_ptr(s, 3) + koff);
-                            tc_mma_tf32(d, ahi, blo, acc_in);
-                            tc_mma_tf32(d, alo, bhi, 1u);
-                            tc_mma_tf32(d, ahi, bhi, 1u);
-                        } else if (KIND == kBf16) {
-                            tc_mma_bf16(d, ahi, bhi, acc_in);
-                        } else {
-                            tc_mma_tf32(d, ahi, bhi, acc_in);
+            uint32_t g = 0;    // k-tiles consumed, over all tiles
+            uint32_t gc = 0;   // accumulation chunks issued, over all tiles
+            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                for (int c = 0; c < nchunks && ok; ++c, ++gc) {
+                    const int b = (int)(gc & 1);
+                    if (gc >= 2) {   // the epilogue must have read this buffer's previous chunk
+                        if (!mbar_wait(smem_u32(&cempty[b]), ((gc >> 1) - 1) & 1, wait_ns)) {
+                            ok = false;
+                            break;
                         }
+                        tc_fence_after();
                     }
-                    issued_any = true;
-                    tc_commit(smem_u32(&empty[s]));   // the stage is free once these MMAs are done
+                    const uint32_t d = tmem + (uint32_t)(b * TBN);
+                    const int kt_end = (c + 1) * L::KC < ktiles ? (c + 1) * L::KC : ktiles;
+                    for (int kt = c * L::KC; kt < kt_end; ++kt) {
+                        const int s = (int)(g % TSTG);
+                        if (!mbar_wait(smem_u32(&full[s]), (g / TSTG) & 1, wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < KT / L::MMA_K; ++kk) {
+                            const uint32_t koff = kk * 32;   // 8 TF32 or 16 BF16 = 32 bytes along K
+                            const uint64_t ahi = smem_desc<L::SWB>(stage_ptr(s, 0) + koff);
+                            const uint64_t bhi = smem_desc<L::SWB>(stage_ptr(s, 2) + koff);
+                            const uint32_t acc_in = (kt != c * L::KC || kk != 0) ? 1u : 0u;
+                            if (TERMS == 3) {
+                                const uint64_t alo = smem_desc<L::SWB>(stage_ptr(s, 1) + koff);
+                                const uint64_t blo = smem_desc<L::SWB>(stage_ptr(s, 3) + koff);
+                                tc_mma_tf32(d, ahi, blo, acc_in);
+                                tc_mma_tf32(d, alo, bhi, 1u);
+                                tc_mma_tf32(d, ahi, bhi, 1u);
+                            } else if (KIND == kBf16) {
+                                tc_mma_bf16(d, ahi, bhi, acc_in);
+                            } else {
+                                tc_mma_tf32(d, ahi, bhi, acc_in);
+                            }
+                        }
+                        issued_any = true;
+                        tc_commit(smem_u32(&empty[s]));   // the stage is free once these MMAs are done
+                        ++g;
+                    }
+                    if (ok) tc_commit(smem_u32(&cfull[b]));
                 }
-                if (ok) tc_commit(smem_u32(&cfull[b]));
             }
             if (!ok) {
                 record_error(err, kErrWaitTimeout);
@@ -324,43 +344,48 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
         }
     } else {
         // Epilogue warp w: tensor-memory lanes (rows) 32*(w%4) .. +31,
-        // columns (w/4)*EPI_COLS .. +EPI_COLS.
+        // columns (w/4)*EPI_COLS .. +EPI_COLS.  The store of one tile runs
+        // while the MMAs of the next tile fill the other accumulator buffer.
         const int lane_base = (warp & 3) * 32;
         const int col_base = (warp >> 2) * EPI_COLS;
-        float acc[EPI_COLS];
-#pragma unroll
-        for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+        const bool tail = ep.bias != nullptr || ep.act != kActNone;
         bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int b = c & 1;
-            // tcgen05.ld is warp-collective: lane 0 decides for the warp whether
-            // the chunk is ready; the others then see the completed phase at once.
-            bool ready = lane == 0 ? mbar_wait(smem_u32(&cfull[b]), (c >> 1) & 1, wait_ns) : false;
-            ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-            if (!ready) {
-                ok = false;
-                break;
-            }
-            mbar_wait(smem_u32(&cfull[b]), (c >> 1) & 1, DRAIN_NS);
-            tc_fence_after();
-            const uint32_t taddr = tmem + ((uint32_t)lane_base << 16) + (uint32_t)(b * TBN + col_base);
+        uint32_t gc = 0;   // chunks drained, over all tiles
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            int m0, n0;
+            tile_origin(t, m0, n0);
+            float acc[EPI_COLS];
 #pragma unroll
-            for (int piece = 0; piece < EPI_COLS / 16; ++piece) {
-                float v[16];
+            for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+            for (int c = 0; c < nchunks; ++c, ++gc) {
+                const int b = (int)(gc & 1);
+                // tcgen05.ld is warp-collective: lane 0 decides for the warp whether
+                // the chunk is ready; the others then see the completed phase at once.
+                bool ready =
+                    lane == 0 ? mbar_wait(smem_u32(&cfull[b]), (gc >> 1) & 1, wait_ns) : false;
+                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+                if (!ready) {
+                    ok = false;
+                    break;
+                }
+                mbar_wait(smem_u32(&cfull[b]), (gc >> 1) & 1, DRAIN_NS);
+                tc_fence_after();
+                const uint32_t taddr =
+                    tmem + ((uint32_t)lane_base << 16) + (uint32_t)(b * TBN + col_base);
+#pragma unroll
+                for (int piece = 0; piece < EPI_COLS / 16; ++piece) {
+                    float v[16];
+                    __syncwarp();
+                    tc_ld16(taddr + (uint32_t)(piece * 16), v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[piece * 16 + i] += v[i];
+                }
+                tc_fence_before();
                 __syncwarp();
-                tc_ld16(taddr + (uint32_t)(piece * 16), v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) acc[piece * 16 + i] += v[i];
+                if (lane == 0) mbar_arrive(smem_u32(&cempty[b]));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&cempty[b]));
-        }
-        if (!ok) {
-            if (lane == 0) record_error(err, kErrWaitTimeout);
-        } else {
+            if (!ok) break;
             const int gm = m0 + lane_base + lane;
-            const bool tail = ep.bias != nullptr || ep.act != kActNone;
             if (gm < M) {
                 float *crow = C + (int64_t)gm * ldc;
 #pragma unroll
@@ -396,6 +421,7 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
                 }
             }
         }
+        if (!ok && lane == 0) record_error(err, kErrWaitTimeout);
     }
 
     tc_fence_before();
@@ -421,7 +447,10 @@ cudaError_t launch_mma(const GemmArgs &g, const CUtensorMap &tAhi, const CUtenso
     if (e != cudaSuccess) return e;
     const int64_t tiles = ((g.N + TBN - 1) / TBN) * ((g.M + TBM - 1) / TBM);
     if (tiles > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const dim3 grid((unsigned)tiles);
+    // Persistent: one CTA per SM (the 192 KB ring allows one), each walking
+    // its share of the tiles; TF_PERSIST=0 launches one CTA per tile instead.
+    const int64_t ctas = TF_PERSIST && g.sm_count > 0 && g.sm_count < tiles ? g.sm_count : tiles;
+    const dim3 grid((unsigned)ctas);
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
     tf32_mma_kernel<TERMS, KIND><<<grid, THREADS, L::SMEM, g.stream>>>(
         tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N, (int)g.K, g.epi(), g.C, g.ldc, c_vec4,
@@ -499,7 +528,8 @@ size_t tf32_workspace_floats(int64_t M, int64_t N, int64_t K, int terms) {
 
 bool tf32x3_can_run(int64_t M, int64_t N, int64_t K) {
     const int64_t lim = int64_t(1) << 31;
-    return M < lim && N < lim && K < lim && ((M + TBM - 1) / TBM) * ((N + TBN - 1) / TBN) <= 0x7fffffff &&
+    // the tile index (plus one grid stride) stays an int
+    return M < lim && N < lim && K < lim && ((M + TBM - 1) / TBM) * ((N + TBN - 1) / TBN) <= 0x7fff0000 &&
            (K + 31) / 32 <= 65535;
 }
 
