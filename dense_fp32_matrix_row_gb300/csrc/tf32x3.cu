@@ -14,21 +14,26 @@
 //  1. split kernels (memory-bound) write A_hi, A_lo as [M][K] and B_hi, B_lo
 //     transposed as [N][K] into the workspace, so both MMA operands are
 //     K-major -- the canonical UMMA layout;
-//  2. the MMA kernel: one CTA per 128 x 256 tile of C.  Warp 8 streams 16-wide
-//     K slices of the four operand tiles into a 4-stage shared-memory ring
-//     with TMA (64-byte swizzle; the one-term kinds below stream 128-byte K
-//     rows with the 128-byte swizzle); one thread of warp 9 issues, per 8-wide k
-//     step, three tcgen05.mma kind::tf32 (hi*lo, lo*hi, hi*hi) into one FP32
-//     accumulator of 128 lanes x 256 columns in tensor memory and releases
-//     each stage with tcgen05.commit; warps 0-7 read the accumulator back with
-//     tcgen05.ld (each warp 32 lanes = rows, half the columns), add it into
-//     FP32 registers chunk by chunk (see tf32x3_kernel) and finally apply
-//     C = alpha*acc + beta*C, reading C only when beta != 0.
+//  2. the MMA kernel, persistent (one CTA per SM walking its tiles), on one
+//     SM per 128 x 256 tile (tf32_mma_kernel) or, for M >= 256, on a pair of
+//     SMs per 256 x 256 tile with tcgen05 cta_group::2 (tf32_mma2_kernel, see
+//     there).  Warp 8 streams 16-wide K slices of the four operand tiles into
+//     a shared-memory ring with TMA (64-byte swizzle; the one-term kinds below
+//     stream 128-byte K rows with the 128-byte swizzle); one thread of warp 9
+//     issues, per 8-wide k step, three tcgen05.mma kind::tf32 (hi*lo, lo*hi,
+//     hi*hi) into an FP32 accumulator of 128 lanes x 256 columns in tensor
+//     memory and releases each stage with tcgen05.commit; warps 0-7 read the
+//     accumulator back with tcgen05.ld (each warp 32 lanes = rows, half the
+//     columns), add it into FP32 registers chunk by chunk (see
+//     tf32_mma_kernel) and finally apply C = alpha*acc + beta*C, reading C
+//     only when beta != 0.
 //
 // Every wait is bounded.  On a time-out the kernel records the error, waits
 // (bounded) for its own TMA copies and MMAs in flight, frees its tensor
 // memory and exits without storing.
 #include <cuda_bf16.h>
+
+#include <atomic>
 
 #include "common.cuh"
 
@@ -36,16 +41,25 @@ namespace sgemm_gb300 {
 namespace {
 
 constexpr int TBM = 128, TBN = 256;
-constexpr int KC_TILES = 4;                     // 3xTF32: k-tiles per accumulation chunk (64 k)
-// One-term kinds: 512 k (TF32) / 1024 k (BF16) per chunk.  A 64 k chunk is
+#ifndef TF_KC3
+#define TF_KC3 6
+#endif
+// 3xTF32: k-tiles per accumulation chunk (96 k).  Shorter chunks keep the
+// tensor-memory accumulation error lower but make the MMAs wait for the
+// epilogue warps of both SMs between chunks; measured at 8192^3 (two-SM
+// tiles): 64 k 290 TFLOP/s, 96 k 321, 128 k 327, with the mean relative
+// error 4.7e-7 at 64 k and 9.1e-7 at 128 k (FP32 FFMA: 2e-7 .. 4e-7).
+constexpr int KC_TILES = TF_KC3;
+// One-term kinds: 1024 k (TF32) / 2048 k (BF16) per chunk.  A 64 k chunk is
 // only 8 MMAs, about as long as the epilogue warps take to drain a 128 x 256
 // accumulator from tensor memory, so the MMAs waited on the drain.  Measured
 // at 8192^3 (TFLOP/s / normwise error against the rounded-operand product,
 // TF32 and BF16): 64 k 463 / 1.0e-8 and 814 / 7e-9; 256 k 557 / 1.5e-8 and
-// 959 / 9e-9 (64-byte rows, one CTA per tile); in the persistent kernel with
-// 128-byte rows 256 k 718 and 1240, 512 k 741 / 2.4e-8 and 1282 / 1.7e-8.
+// 959 / 9e-9 (64-byte rows, one CTA per tile); persistent, 128-byte rows:
+// 256 k 718 and 1240, 512 k 741 / 2.4e-8 and 1282 / 1.7e-8; two-SM tiles:
+// 512 k 767 and 1286, 1024 k 807 / 4.4e-8 and 1364 / 4.1e-8.
 #ifndef TF_KC1
-#define TF_KC1 32   // in 64-byte k-tiles (512 k TF32, 1024 k BF16); scaled to the row width used
+#define TF_KC1 64   // in 64-byte k-tiles (1024 k TF32, 2048 k BF16); scaled to the row width used
 #endif
 // Swizzle span (= bytes of K per operand row of a stage) of the one-term
 // kinds.  128-byte rows move each stage in half as many TMA requests as
@@ -53,6 +67,9 @@ constexpr int KC_TILES = 4;                     // 3xTF32: k-tiles per accumulat
 // 3-term kind by the tensor pipe, so only the former use them.
 #ifndef TF_SW1
 #define TF_SW1 128
+#endif
+#ifndef TF_PAIR
+#define TF_PAIR 1   // two-SM (cta_group::2) tiles for M >= 256
 #endif
 #ifndef TF_PERSIST
 #define TF_PERSIST 1
@@ -436,6 +453,391 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
 }
 
 
+// ---------------------------------------------------------------------------
+// Two-SM tiles (tcgen05 cta_group::2).  A cluster of two CTAs on two SMs owns
+// a 256 x 256 tile of C.  Each CTA stages its own 128 rows of A and half of
+// the tile's B (128 of the 256 columns); one thread of the even CTA issues
+// tcgen05.mma.cta_group::2 with M = 256, which reads A and B from both CTAs'
+// shared memory at the same offsets and writes each CTA's 128 rows of the
+// accumulator into that CTA's tensor memory.  Per SM this moves a third fewer
+// operand bytes per MMA than the one-SM 128 x 256 tile, so the same 192 KB
+// ring holds six stages instead of four.
+//
+// Synchronisation (all barriers at the same offsets in both CTAs):
+//   full[s]    even CTA: both CTAs' TMA bytes of stage s landed (the odd
+//              CTA's copies complete on it through the cta_group::2 form)
+//   empty[s]   both: the MMAs reading stage s are done (multicast commit)
+//   cfull[b]   both: accumulator buffer b holds a finished chunk (multicast commit)
+//   cempty[b]  even CTA: all 16 epilogue warps of the pair have read buffer b
+// Every wait is bounded; a time-out is recorded and the roles wind down.
+
+template <int TERMS, int KIND>
+struct PairCfg {
+    using One = TfCfg<TERMS, KIND>;
+    static constexpr int PARTS = One::PARTS, SWB = One::SWB, KT = One::KT, MMA_K = One::MMA_K,
+                         KC = One::KC;
+    static constexpr int HALF_N = TBN / 2;                       // B columns held per CTA
+    static constexpr uint32_t A_TILE = TBM * SWB, B_TILE = HALF_N * SWB;
+    static constexpr uint32_t STAGE_BYTES = PARTS * (A_TILE + B_TILE);
+    static constexpr int TSTG = (192 * 1024) / STAGE_BYTES;
+    // SLACK after the ring keeps any operand read that starts inside the ring
+    // (a tile of up to 256 rows) inside this CTA's shared memory.
+    static constexpr uint32_t SLACK = PARTS * B_TILE;
+    static constexpr size_t SMEM = 1024 + (size_t)TSTG * STAGE_BYTES + SLACK + 512;
+    static_assert(A_TILE % 1024 == 0 && B_TILE % 1024 == 0, "tiles keep 1024-byte alignment");
+    static_assert(SMEM <= 227 * 1024, "shared memory per block");
+};
+
+// Instruction descriptors with M = 256 (the pair's rows).
+constexpr uint32_t IDESC2 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(TBN >> 3) << 17) |
+                            ((uint32_t)(256 >> 4) << 24);
+constexpr uint32_t IDESC2_BF16 = (1u << 4) | (BF16_FORMAT << 7) | (BF16_FORMAT << 10) |
+                                 ((uint32_t)(TBN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+
+__device__ __forceinline__ void tc2_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate, bool bf16) {
+    if (bf16)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+}
+
+// Arrive on the barrier at offset `bar` in both CTAs of the pair once every
+// tcgen05 operation this thread issued so far is done.
+__device__ __forceinline__ void tc2_commit_both(uint32_t bar) {
+    const uint16_t mask = 0x3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+        "[%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+// 2-D TMA load into this CTA's shared memory that completes its bytes on a
+// barrier that may belong to the peer CTA of the pair (`bar` a shared::cluster
+// address, e.g. from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                                 int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t bar, uint32_t cta) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(cta));
+    return remote;
+}
+
+// Arrive (release, cluster scope) on the barrier at offset `bar` of CTA `cta`.
+__device__ __forceinline__ void mbar_arrive_cta(uint32_t bar, uint32_t cta) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(bar), "r"(cta));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote)
+                 : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (for barriers other CTAs arrive on).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    auto try_once = [&]() {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        return ok != 0;
+    };
+    if (try_once()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (try_once()) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+template <int TERMS, int KIND>
+__global__ void __launch_bounds__(THREADS, 1)
+tf32_mma2_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
+                 const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
+                 int M, int N, int K, Epilogue ep, float *__restrict__ C, int64_t ldc,
+                 int c_vec4, unsigned *err, uint64_t wait_ns) {
+    using L = PairCfg<TERMS, KIND>;
+    constexpr int TSTG = L::TSTG;
+    constexpr int KT = L::KT;
+    constexpr uint32_t STAGE_BYTES = L::STAGE_BYTES;
+    extern __shared__ unsigned char smem_raw[];
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+    unsigned char *ring = reinterpret_cast<unsigned char *>(base);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)TSTG * STAGE_BYTES + L::SLACK);
+    uint64_t *empty = full + TSTG;
+    uint64_t *cfull = empty + TSTG;
+    uint64_t *cempty = cfull + 2;
+    uint64_t *drainbar = cempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drainbar + 1);
+
+    uint32_t rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    const bool lead = rank == 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Persistent over pair tiles: cluster p takes tiles p, p + #clusters, ...
+    const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+    const int num_m = (M + 2 * TBM - 1) / (2 * TBM), num_n = (N + TBN - 1) / TBN;
+    const int tiles = num_m * num_n;
+    const int per_group = RASTER_GROUP * num_n;
+    auto tile_origin = [&](int t, int &m0, int &n0) {
+        const int first_m = (t / per_group) * RASTER_GROUP;
+        const int gsz = (num_m - first_m) < RASTER_GROUP ? (num_m - first_m) : RASTER_GROUP;
+        m0 = (first_m + (t % per_group) % gsz) * (2 * TBM);
+        n0 = ((t % per_group) / gsz) * TBN;
+    };
+    const int ktiles = (K + KT - 1) / KT;
+    const int nchunks = (ktiles + L::KC - 1) / L::KC;
+    auto stage_ptr = [&](int s, int which) -> uint32_t {   // 0 A_hi, 1 A_lo, 2 B_hi, 3 B_lo
+        constexpr int P = L::PARTS;
+        const uint32_t off =
+            which < 2 ? which * L::A_TILE : P * L::A_TILE + (which - 2) * L::B_TILE;
+        return smem_u32(ring + (size_t)s * STAGE_BYTES + off);
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < TSTG; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&cfull[b]), 1);
+            mbar_init(smem_u32(&cempty[b]), 2 * EPI_WARPS);
+        }
+        mbar_init(smem_u32(drainbar), 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) {   // one warp of each CTA: the pair allocates its columns together
+        __syncwarp();
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // both CTAs' barriers exist before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    if (warp == PRODUCER_WARP) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmAhi);
+            tma_prefetch_desc(&tmBhi);
+            if (TERMS == 3) {
+                tma_prefetch_desc(&tmAlo);
+                tma_prefetch_desc(&tmBlo);
+            }
+            uint32_t g = 0;
+            bool ok = true;
+            for (int t = pair; t < tiles && ok; t += npairs) {
+                int m0, n0;
+                tile_origin(t, m0, n0);
+                const int ya = m0 + TBM * (int)rank, yb = n0 + L::HALF_N * (int)rank;
+                for (int kt = 0; kt < ktiles; ++kt) {
+                    const int s = (int)(g % TSTG);
+                    const uint32_t use = g / TSTG;
+                    if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    // both CTAs' bytes complete on the even CTA's full[s]
+                    const uint32_t fb = cluster_addr(smem_u32(&full[s]), 0);
+                    if (lead) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * STAGE_BYTES);
+                    tma_load_2d_pair(stage_ptr(s, 0), &tmAhi, fb, kt * KT, ya);
+                    tma_load_2d_pair(stage_ptr(s, 2), &tmBhi, fb, kt * KT, yb);
+                    if (TERMS == 3) {
+                        tma_load_2d_pair(stage_ptr(s, 1), &tmAlo, fb, kt * KT, ya);
+                        tma_load_2d_pair(stage_ptr(s, 3), &tmBlo, fb, kt * KT, yb);
+                    }
+                    ++g;
+                }
+            }
+            if (!ok) {
+                record_error(err, kErrWaitTimeout);
+                if (lead)   // the odd CTA's copies complete on these barriers too
+                    for (uint32_t q = (g > TSTG ? g - TSTG : 0); q < g; ++q)
+                        mbar_wait(smem_u32(&full[q % TSTG]), (q / TSTG) & 1, DRAIN_NS);
+            }
+        }
+    } else if (warp == MMA_WARP) {
+        if (lane == 0 && lead) {
+            bool ok = true;
+            bool issued_any = false;
+            uint32_t g = 0, gc = 0;
+            constexpr uint32_t idesc = KIND == kBf16 ? IDESC2_BF16 : IDESC2;
+            for (int t = pair; t < tiles && ok; t += npairs) {
+                for (int c = 0; c < nchunks && ok; ++c, ++gc) {
+                    const int b = (int)(gc & 1);
+                    if (gc >= 2) {   // both CTAs' epilogues must have read this buffer
+                        if (!mbar_wait_cluster(smem_u32(&cempty[b]), ((gc >> 1) - 1) & 1, wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint32_t d = tmem + (uint32_t)(b * TBN);
+                    const int kt_end = (c + 1) * L::KC < ktiles ? (c + 1) * L::KC : ktiles;
+                    for (int kt = c * L::KC; kt < kt_end; ++kt) {
+                        const int s = (int)(g % TSTG);
+                        if (!mbar_wait_cluster(smem_u32(&full[s]), (g / TSTG) & 1, wait_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < KT / L::MMA_K; ++kk) {
+                            const uint32_t koff = kk * 32;
+                            const uint64_t ahi = smem_desc<L::SWB>(stage_ptr(s, 0) + koff);
+                            const uint64_t bhi = smem_desc<L::SWB>(stage_ptr(s, 2) + koff);
+                            const uint32_t acc_in = (kt != c * L::KC || kk != 0) ? 1u : 0u;
+                            if (TERMS == 3) {
+                                const uint64_t alo = smem_desc<L::SWB>(stage_ptr(s, 1) + koff);
+                                const uint64_t blo = smem_desc<L::SWB>(stage_ptr(s, 3) + koff);
+                                tc2_mma(d, ahi, blo, idesc, acc_in, false);
+                                tc2_mma(d, alo, bhi, idesc, 1u, false);
+                                tc2_mma(d, ahi, bhi, idesc, 1u, false);
+                            } else {
+                                tc2_mma(d, ahi, bhi, idesc, acc_in, KIND == kBf16);
+                            }
+                        }
+                        issued_any = true;
+                        tc2_commit_both(smem_u32(&empty[s]));   // both CTAs may refill stage s
+                        ++g;
+                    }
+                    if (ok) tc2_commit_both(smem_u32(&cfull[b]));
+                }
+            }
+            if (!ok) {
+                record_error(err, kErrWaitTimeout);
+                if (issued_any) {
+                    asm volatile(
+                        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                            smem_u32(drainbar))
+                        : "memory");
+                    mbar_wait(smem_u32(drainbar), 0, DRAIN_NS);
+                }
+            }
+        }
+    } else {
+        // Epilogue warp w of CTA r: rows m0 + 128 r + 32 (w % 4) + lane (this
+        // CTA's tensor-memory lanes), columns (w / 4) * EPI_COLS .. + EPI_COLS.
+        const int lane_base = (warp & 3) * 32;
+        const int col_base = (warp >> 2) * EPI_COLS;
+        const bool tail = ep.bias != nullptr || ep.act != kActNone;
+        bool ok = true;
+        uint32_t gc = 0;
+        for (int t = pair; t < tiles && ok; t += npairs) {
+            int m0, n0;
+            tile_origin(t, m0, n0);
+            float acc[EPI_COLS];
+#pragma unroll
+            for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+            for (int c = 0; c < nchunks; ++c, ++gc) {
+                const int b = (int)(gc & 1);
+                bool ready =
+                    lane == 0 ? mbar_wait(smem_u32(&cfull[b]), (gc >> 1) & 1, wait_ns) : false;
+                ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+                if (!ready) {
+                    ok = false;
+                    break;
+                }
+                mbar_wait(smem_u32(&cfull[b]), (gc >> 1) & 1, DRAIN_NS);
+                tc_fence_after();
+                const uint32_t taddr =
+                    tmem + ((uint32_t)lane_base << 16) + (uint32_t)(b * TBN + col_base);
+#pragma unroll
+                for (int piece = 0; piece < EPI_COLS / 16; ++piece) {
+                    float v[16];
+                    __syncwarp();
+                    tc_ld16(taddr + (uint32_t)(piece * 16), v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[piece * 16 + i] += v[i];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(smem_u32(&cempty[b]), 0);
+            }
+            if (!ok) break;
+            const int gm = m0 + TBM * (int)rank + lane_base + lane;
+            if (gm < M) {
+                float *crow = C + (int64_t)gm * ldc;
+#pragma unroll
+                for (int q = 0; q < EPI_COLS / 4; ++q) {
+                    const int gn = n0 + col_base + 4 * q;
+                    float o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = ep.alpha * acc[4 * q + e];
+                    if (c_vec4 && gn + 3 < N) {
+                        float4 *p = reinterpret_cast<float4 *>(crow + gn);
+                        if (ep.beta != 0.0f) {
+                            const float4 cv = *p;
+                            o[0] = fmaf(ep.beta, cv.x, o[0]);
+                            o[1] = fmaf(ep.beta, cv.y, o[1]);
+                            o[2] = fmaf(ep.beta, cv.z, o[2]);
+                            o[3] = fmaf(ep.beta, cv.w, o[3]);
+                        }
+                        if (tail) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) o[e] = epilogue_tail(ep, o[e], gn + e);
+                        }
+                        *p = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (gn + e < N) {
+                                float *p = crow + gn + e;
+                                const float w = (ep.beta != 0.0f) ? fmaf(ep.beta, *p, o[e]) : o[e];
+                                *p = tail ? epilogue_tail(ep, w, gn + e) : w;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) record_error(err, kErrWaitTimeout);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // the pair is done with each other's memory and barriers
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+
 int64_t tf32_ld(int64_t K) { return (K + 3) / 4 * 4; }
 
 template <int TERMS, int KIND>
@@ -458,6 +860,52 @@ cudaError_t launch_mma(const GemmArgs &g, const CUtensorMap &tAhi, const CUtenso
     return cudaGetLastError();
 }
 
+// Two-SM tiles: clusters of two CTAs, as many as fit at once (one CTA per
+// SM), each walking its share of the 256 x 256 tiles.  Returns
+// cudaErrorNotSupported (nothing launched) when no cluster fits.
+template <int TERMS, int KIND>
+cudaError_t launch_mma2(const GemmArgs &g, const CUtensorMap &tAhi, const CUtensorMap &tAlo,
+                        const CUtensorMap &tBhi, const CUtensorMap &tBlo) {
+    using L = PairCfg<TERMS, KIND>;
+    static std::atomic<int> max_pairs[64];   // per device, +1 (0: not yet known)
+    auto kern = tf32_mma2_kernel<TERMS, KIND>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cfg.stream = g.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int np = max_pairs[dev].load(std::memory_order_relaxed) - 1;
+    if (np < 0) {
+        cfg.gridDim = dim3(2, 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&np, kern, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            np = 0;
+        }
+        max_pairs[dev].store(np + 1, std::memory_order_relaxed);
+    }
+    if (np <= 0) return cudaErrorNotSupported;
+
+    const int64_t tiles = ((g.N + TBN - 1) / TBN) * ((g.M + 2 * TBM - 1) / (2 * TBM));
+    const int64_t pairs = tiles < np ? tiles : np;
+    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+    const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
+    return cudaLaunchKernelEx(&cfg, kern, tAhi, tAlo, tBhi, tBlo, (int)g.M, (int)g.N, (int)g.K,
+                              g.epi(), g.C, g.ldc, c_vec4, g.err, g.wait_ns);
+}
+
+// Whether a product runs on two-SM tiles: at least one full pair of rows.
+bool use_pairs(int64_t M) { return TF_PAIR && M >= 2 * TBM; }
+
 int64_t bf16_ld(int64_t K) { return (K + 7) / 8 * 8; }
 
 template <int TERMS>
@@ -479,16 +927,24 @@ cudaError_t launch_terms(const GemmArgs &g, float *ws) {
     alignas(64) CUtensorMap tAhi, tAlo, tBhi, tBlo;
     const CUtensorMapSwizzle sw = L::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     constexpr uint32_t kt = L::KT;
-    if (!encode_tma_2d(g.encode, &tAhi, ahi, g.K, g.M, ldk, kt, TBM, sw) ||
-        !encode_tma_2d(g.encode, &tBhi, bhi, g.K, g.N, ldk, kt, TBN, sw))
-        return cudaErrorInvalidValue;
-    if (TERMS == 3) {
-        if (!encode_tma_2d(g.encode, &tAlo, alo, g.K, g.M, ldk, kt, TBM, sw) ||
-            !encode_tma_2d(g.encode, &tBlo, blo, g.K, g.N, ldk, kt, TBN, sw))
+    for (int pass = use_pairs(g.M) ? 0 : 1; pass < 2; ++pass) {
+        // pass 0: two-SM tiles (each CTA holds half of B's 256 columns); pass 1: one-SM tiles
+        const uint32_t brows = pass == 0 ? TBN / 2 : TBN;
+        if (!encode_tma_2d(g.encode, &tAhi, ahi, g.K, g.M, ldk, kt, TBM, sw) ||
+            !encode_tma_2d(g.encode, &tBhi, bhi, g.K, g.N, ldk, kt, brows, sw))
             return cudaErrorInvalidValue;
-    } else {
-        tAlo = tAhi;   // never read
-        tBlo = tBhi;
+        if (TERMS == 3) {
+            if (!encode_tma_2d(g.encode, &tAlo, alo, g.K, g.M, ldk, kt, TBM, sw) ||
+                !encode_tma_2d(g.encode, &tBlo, blo, g.K, g.N, ldk, kt, brows, sw))
+                return cudaErrorInvalidValue;
+        } else {
+            tAlo = tAhi;   // never read
+            tBlo = tBhi;
+        }
+        if (pass == 0) {
+            e = launch_mma2<TERMS, kTf32>(g, tAhi, tAlo, tBhi, tBlo);
+            if (e != cudaErrorNotSupported) return e;
+        }
     }
     return launch_mma<TERMS, kTf32>(g, tAhi, tAlo, tBhi, tBlo);
 }
@@ -507,9 +963,16 @@ cudaError_t launch_bf16_terms(const GemmArgs &g, float *ws) {
     using L = TfCfg<1, kBf16>;
     const CUtensorMapSwizzle sw = L::SWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     constexpr uint32_t kt = L::KT;
-    if (!encode_tma_2d_bf16(g.encode, &tA, a, g.K, g.M, ldk, kt, TBM, sw) ||
-        !encode_tma_2d_bf16(g.encode, &tB, b, g.K, g.N, ldk, kt, TBN, sw))
-        return cudaErrorInvalidValue;
+    for (int pass = use_pairs(g.M) ? 0 : 1; pass < 2; ++pass) {
+        const uint32_t brows = pass == 0 ? TBN / 2 : TBN;
+        if (!encode_tma_2d_bf16(g.encode, &tA, a, g.K, g.M, ldk, kt, TBM, sw) ||
+            !encode_tma_2d_bf16(g.encode, &tB, b, g.K, g.N, ldk, kt, brows, sw))
+            return cudaErrorInvalidValue;
+        if (pass == 0) {
+            e = launch_mma2<1, kBf16>(g, tA, tA, tB, tB);
+            if (e != cudaErrorNotSupported) return e;
+        }
+    }
     return launch_mma<1, kBf16>(g, tA, tA, tB, tB);
 }
 
