@@ -682,9 +682,17 @@ tf32_mma2_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constan
             }
             if (!ok) {
                 record_error(err, kErrWaitTimeout);
-                if (lead)   // the odd CTA's copies complete on these barriers too
+                if (lead) {   // the odd CTA's copies complete on these barriers too
                     for (uint32_t q = (g > TSTG ? g - TSTG : 0); q < g; ++q)
                         mbar_wait(smem_u32(&full[q % TSTG]), (q / TSTG) & 1, DRAIN_NS);
+                } else {
+                    // The odd CTA cannot wait on its copies (they complete on the
+                    // even CTA's barriers, possibly in phases the even CTA gave up
+                    // on): give them time to land before the CTA can exit.
+                    const uint64_t t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 200000ull) {
+                    }
+                }
             }
         }
     } else if (warp == MMA_WARP) {

@@ -323,6 +323,22 @@ def test_tf32x3_nan_propagates():
     assert np.isnan(C[7]).all() and np.isfinite(np.delete(C, 7, axis=0)).all()
 
 
+# ---------------------------------------------------------------- two-SM tensor-core tiles
+# M >= 256 runs on clusters of two CTAs (tcgen05 cta_group::2), each pair a
+# 256 x 256 tile: exactly one pair tile, a second pair tile whose odd CTA
+# holds no rows (M = 257) or whose rows are all past M (M = 384), B halves
+# partly or wholly past N, K tails, more tiles than co-resident pairs (the
+# persistent loop), and M = 255 (still one-SM tiles) for contrast.
+@pytest.mark.parametrize("mode", [sg.MODE_3XTF32, sg.MODE_TF32, sg.MODE_BF16])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 16), (257, 300, 100), (384, 129, 33), (512, 1, 40),
+                                   (255, 260, 70), (2048, 2560, 64)])
+def test_pair_tiles(mode, M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "uniform", seed=M + 3 * N + 7 * K + mode, beta=-0.75)
+    kid = {sg.MODE_3XTF32: TF, sg.MODE_TF32: sg.KERNEL_TF32, sg.MODE_BF16: sg.KERNEL_BF16}[mode]
+    _, chosen = run_checked(sg, A, B, C0, 1.5, -0.75, tensor_cores=mode)
+    assert chosen == kid
+
+
 # ---------------------------------------------------------------- FFMA tile configurations
 # Every configuration compiled into the library (the autotuner's choices),
 # forced, on shapes with ragged edges, a split last wave and beta != 0.
