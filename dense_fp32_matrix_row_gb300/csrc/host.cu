@@ -26,6 +26,7 @@ using namespace sgemm_gb300;
 namespace {
 
 constexpr int kSlots = 2;
+constexpr int kBParts = 4;   // most K-ranges B arrives in while the first panel computes
 constexpr size_t kAlign = 256;   // bytes; every device sub-buffer starts on this boundary
 
 struct HostPath {
@@ -35,6 +36,7 @@ struct HostPath {
     cudaStream_t down = nullptr;   // device -> host copies
     cudaEvent_t fork = nullptr, join = nullptr;
     cudaEvent_t loaded[kSlots] = {}, computed[kSlots] = {}, stored[kSlots] = {};
+    cudaEvent_t bpart[kBParts] = {};   // rows of B up to K-range j are on the device
     void *buf = nullptr;           // device buffer: B, then kSlots x (A panel, C panel)
     size_t bytes = 0;
 };
@@ -55,6 +57,8 @@ int create(HostPath &h) {
         ok = cudaEventCreateWithFlags(&h.loaded[s], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&h.computed[s], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&h.stored[s], cudaEventDisableTiming) == cudaSuccess;
+    for (int j = 0; ok && j < kBParts; ++j)
+        ok = cudaEventCreateWithFlags(&h.bpart[j], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
         (void)cudaGetLastError();
         return SGEMM_ERR_CUDA;
@@ -72,12 +76,28 @@ void destroy(HostPath &h) {
     for (int s = 0; s < kSlots; ++s)
         for (cudaEvent_t e : {h.loaded[s], h.computed[s], h.stored[s]})
             if (e != nullptr) (void)cudaEventDestroy(e);
+    for (int j = 0; j < kBParts; ++j)
+        if (h.bpart[j] != nullptr) (void)cudaEventDestroy(h.bpart[j]);
     h.buf = nullptr;
     h.bytes = 0;
     h.ready = false;
     h.up = h.down = nullptr;
     h.fork = h.join = nullptr;
     for (int s = 0; s < kSlots; ++s) h.loaded[s] = h.computed[s] = h.stored[s] = nullptr;
+    for (int j = 0; j < kBParts; ++j) h.bpart[j] = nullptr;
+}
+
+// K-ranges the first panel is computed in, so that the copy of B (which the
+// first panel needs in full) overlaps the first panel's products: B goes up
+// range by range after A_0 and C_0, and range j is multiplied as soon as it
+// has arrived (C_0 = alpha*A_0[:, range 0]@B[range 0] + beta*C_0, then
+// C_0 += alpha*A_0[:, range j]@B[range j]).  Only with several panels and a
+// deep K; one range otherwise.
+int b_parts(int64_t M, int64_t rows, int64_t K, bool uses_ab) {
+    if (!uses_ab || rows >= M) return 1;
+    if (K >= 2048) return kBParts;
+    if (K >= 1024) return 2;
+    return 1;
 }
 
 // Rows per panel.  Panels must stay large enough to fill the GPU on their
@@ -225,10 +245,12 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int
         dC[s] = reinterpret_cast<float *>(base + b_bytes + s * (a_bytes + c_bytes) + a_bytes);
     }
 
+    const int nb = b_parts(M, rows, K, uses_ab);
+    const int64_t kc = (K + nb - 1) / nb;   // rows of B per K-range
     bool ok = cudaEventRecord(h.fork, S) == cudaSuccess &&
               cudaStreamWaitEvent(h.up, h.fork, 0) == cudaSuccess &&
               cudaStreamWaitEvent(h.down, h.fork, 0) == cudaSuccess;
-    if (ok && uses_ab) ok = copy_rows(dB, ldb_d, B, ldb, N, K, h.up);
+    if (ok && uses_ab && nb == 1) ok = copy_rows(dB, ldb_d, B, ldb, N, K, h.up);
     rc = ok ? SGEMM_OK : SGEMM_ERR_CUDA;
     for (int64_t r0 = 0, p = 0; rc == SGEMM_OK && r0 < M; r0 += rows, ++p) {
         const int s = (int)(p % kSlots);
@@ -237,15 +259,35 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int
         if (p >= kSlots) ok = cudaStreamWaitEvent(h.up, h.stored[s], 0) == cudaSuccess;
         if (ok && uses_ab) ok = copy_rows(dA[s], lda_d, A + r0 * lda, lda, K, mp, h.up);
         if (ok && reads_c) ok = copy_rows(dC[s], ldc_d, C + r0 * ldc, ldc, N, mp, h.up);
-        ok = ok && cudaEventRecord(h.loaded[s], h.up) == cudaSuccess &&
-             cudaStreamWaitEvent(S, h.loaded[s], 0) == cudaSuccess;
+        ok = ok && cudaEventRecord(h.loaded[s], h.up) == cudaSuccess;
+        if (p == 0 && nb > 1) {   // B follows A_0 and C_0, one K-range at a time
+            for (int j = 0; ok && j < nb; ++j) {
+                const int64_t k0 = j * kc, kn = std::min(kc, K - k0);
+                ok = copy_rows(dB + k0 * ldb_d, ldb_d, B + k0 * ldb, ldb, N, kn, h.up) &&
+                     cudaEventRecord(h.bpart[j], h.up) == cudaSuccess;
+            }
+        }
+        ok = ok && cudaStreamWaitEvent(S, h.loaded[s], 0) == cudaSuccess;
         if (!ok) {
             rc = SGEMM_ERR_CUDA;
             break;
         }
-        rc = sgemm_fused(mp, N, K, alpha, uses_ab ? dA[s] : nullptr, lda_d,
-                         uses_ab ? dB : nullptr, ldb_d, beta, dC[s], ldc_d, nullptr,
-                         SGEMM_ACT_NONE, mode, stream);
+        if (p == 0 && nb > 1) {
+            for (int j = 0; rc == SGEMM_OK && j < nb; ++j) {
+                const int64_t k0 = j * kc, kn = std::min(kc, K - k0);
+                if (cudaStreamWaitEvent(S, h.bpart[j], 0) != cudaSuccess) {
+                    rc = SGEMM_ERR_CUDA;
+                    break;
+                }
+                rc = sgemm_fused(mp, N, kn, alpha, dA[s] + k0, lda_d, dB + k0 * ldb_d, ldb_d,
+                                 j == 0 ? beta : 1.0f, dC[s], ldc_d, nullptr, SGEMM_ACT_NONE,
+                                 mode, stream);
+            }
+        } else {
+            rc = sgemm_fused(mp, N, K, alpha, uses_ab ? dA[s] : nullptr, lda_d,
+                             uses_ab ? dB : nullptr, ldb_d, beta, dC[s], ldc_d, nullptr,
+                             SGEMM_ACT_NONE, mode, stream);
+        }
         if (rc != SGEMM_OK) break;
         ok = cudaEventRecord(h.computed[s], S) == cudaSuccess &&
              cudaStreamWaitEvent(h.down, h.computed[s], 0) == cudaSuccess &&

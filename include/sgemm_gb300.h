@@ -267,11 +267,16 @@ int sgemm_selftest_wait(int64_t ns, void *stream);
  * double buffering and asynchronous copies hide the loads behind the
  * arithmetic) and queue work asynchronously from the host ("GPU 基础原理",
  * section "3. 第三种区间：开销").  This entry point applies the same overlap one
- * level up, between host and device memory: B is copied to the device, then
- * A and C (C only when beta != 0) follow in row panels on a copy stream;
- * each panel is multiplied on `stream` as soon as it has arrived, and its
- * rows of C go back to the host on a second copy stream while the next
- * panel is multiplied.  Two device slots hold consecutive panels.
+ * level up, between host and device memory: A and C (C only when
+ * beta != 0) go to the device in row panels on a copy stream; each panel is
+ * multiplied on `stream` as soon as it has arrived, and its rows of C go
+ * back to the host on a second copy stream while the next panel is
+ * multiplied.  Two device slots hold consecutive panels.  B travels first
+ * (one panel) or, with several panels and K >= 1024, after A_0 and C_0 in 2
+ * or 4 ranges of K, the first panel being multiplied range by range as B
+ * arrives (C_0 = alpha*A_0 B_0 + beta*C_0, then C_0 += alpha*A_0 B_j): the
+ * result then differs from a single call by the rounding of those partial
+ * sums, within the FP32 accuracy of sgemm().
  *   A, B, C     HOST pointers (device pointers also work: the copies use
  *               cudaMemcpyDefault), row-major with lda, ldb, ldc as in
  *               sgemm().  Page-locked (pinned) host memory lets the copies

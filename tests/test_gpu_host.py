@@ -98,6 +98,23 @@ def test_linear_and_pitched_copies(lds):
     run_host(A, B, C0, 1.0, 0.5, lds=lds, panels=3)
 
 
+@pytest.mark.parametrize("M,N,K,panels", [(700, 300, 1500, 2), (900, 260, 2500, 3),
+                                           (600, 200, 4100, 4)])
+def test_first_panel_in_k_ranges(M, N, K, panels):
+    # with several panels and K >= 1024 the first panel is multiplied in 2 or 4
+    # K-ranges while B is still arriving; beta != 0 and beta == 0 both
+    for beta, seed in ((0.5, 91), (0.0, 92)):
+        A, B, C0 = make_inputs(M, N, K, "normal", seed=seed + K, beta=beta)
+        run_host(A, B, C0, 0.75, beta, panels=panels, lds=(K + 4, N, N))
+
+
+def test_first_panel_in_k_ranges_small_integers_exact():
+    # partial sums of small integers are exact, so splitting K changes nothing
+    M, N, K = 800, 300, 2100
+    A, B, C0 = make_inputs(M, N, K, "int", seed=93, beta=1.0)
+    run_host(A, B, C0, 1.0, 1.0, panels=3, exact=True)
+
+
 def test_default_panel_count_on_a_large_square():
     # the 4092^3 benchmark shape splits into several panels by default; every
     # row is checked against the oracle
