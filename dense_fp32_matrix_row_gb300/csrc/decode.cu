@@ -6,7 +6,11 @@
 // loads that do not allocate in L1, keeps the few rows of A in shared memory,
 // and splits K across the blocks of a thread-block cluster, the split-K idea
 // of "CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section "10" -- but the
-// partial sums are combined on chip instead of by a second reduction kernel:
+// partial sums are combined on chip instead of by a second reduction kernel.
+// Three kernels share that plan: decode_outer_kernel (TMA-staged outer
+// products, every shape whose A and B are 16-byte aligned with ld % 4 == 0;
+// see there), decode_tma_kernel (A unaligned) and, for unaligned B, the
+// plain-load kernel described here:
 //
 //  * grid: (KS, ceil(N/128)); a cluster of KS blocks shares one 128-column
 //    slice of B and C, block `rank` of the cluster takes rows
@@ -744,7 +748,7 @@ cudaError_t launch_tma(const GemmArgs &g) {
 #define DECODE_DW 8
 #endif
 #ifndef DECODE_OUTER_MIN_M
-#define DECODE_OUTER_MIN_M 5
+#define DECODE_OUTER_MIN_M 1
 #endif
 #ifndef DECODE_STAGES
 #define DECODE_STAGES 3
@@ -844,14 +848,13 @@ cudaError_t launch_outer(const GemmArgs &g) {
 
 template <int MT>
 cudaError_t launch_vec(const GemmArgs &g) {
-    if constexpr (MT >= 8) {
-        if (g.M >= DECODE_OUTER_MIN_M && ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) &&
-            (g.ldb % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.A) & 15) == 0) && (g.lda % 4 == 0)) {
-            if constexpr (MT <= 8)
-                return launch_outer<MT, 1>(g);
-            else
-                return launch_outer<MT, 2>(g);
-        }
+    if (g.M >= DECODE_OUTER_MIN_M && ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) &&
+        (g.ldb % 4 == 0) && ((reinterpret_cast<uintptr_t>(g.A) & 15) == 0) && (g.lda % 4 == 0)) {
+        // fewer than 8 rows run the 8-row tile (the copy zero-fills the rows past M)
+        if constexpr (MT <= 8)
+            return launch_outer<8, 1>(g);
+        else
+            return launch_outer<MT, 2>(g);
     }
     const bool vec = ((reinterpret_cast<uintptr_t>(g.B) & 15) == 0) && (g.ldb % 4 == 0);
     if (vec && g.M >= DECODE_TMA_MIN_M)
