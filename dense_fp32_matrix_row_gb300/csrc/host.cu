@@ -295,9 +295,13 @@ int sgemm_host(int64_t M, int64_t N, int64_t K, float alpha, const float *A, int
              cudaEventRecord(h.stored[s], h.down) == cudaSuccess;
         if (!ok) rc = SGEMM_ERR_CUDA;
     }
-    // Join: `stream` waits for the last copy back (and, through the loaded
-    // events, for every copy up), whatever happened above.
-    const bool joined = cudaEventRecord(h.join, h.down) == cudaSuccess &&
+    // Join: `stream` waits for everything enqueued on both copy streams,
+    // whatever happened above (after an error some copies up may not have
+    // been waited for yet), so that later work on `stream` -- a buffer
+    // release or regrowth included -- is ordered after them.
+    const bool joined = cudaEventRecord(h.join, h.up) == cudaSuccess &&
+                        cudaStreamWaitEvent(S, h.join, 0) == cudaSuccess &&
+                        cudaEventRecord(h.join, h.down) == cudaSuccess &&
                         cudaStreamWaitEvent(S, h.join, 0) == cudaSuccess;
     if (rc == SGEMM_OK && !joined) rc = SGEMM_ERR_CUDA;
     if (rc == SGEMM_ERR_CUDA) (void)cudaGetLastError();
