@@ -108,6 +108,15 @@ def test_first_panel_in_k_ranges(M, N, K, panels):
         run_host(A, B, C0, 0.75, beta, panels=panels, lds=(K + 4, N, N))
 
 
+@pytest.mark.parametrize("mode", [sg.MODE_3XTF32, sg.MODE_BF16])
+def test_first_panel_in_k_ranges_tensor_cores(mode):
+    # the K-ranged first panel with the tensor-core arithmetics (each range is
+    # one call of that entry point, so the rounded-operand contracts hold)
+    M, N, K = 640, 384, 2048
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=94 + mode, beta=0.5)
+    run_host(A, B, C0, 1.0, 0.5, mode=mode, panels=2)
+
+
 def test_first_panel_in_k_ranges_small_integers_exact():
     # partial sums of small integers are exact, so splitting K changes nothing
     M, N, K = 800, 300, 2100
