@@ -361,28 +361,33 @@ def test_every_ffma_config(cfg, M, N, K):
 
 # ---------------------------------------------------------------- fused epilogue
 # C = act(alpha*A@B + beta*C + bias[j]) on every kernel path: the TMA tile
-# kernel (whole tiles and a split last wave), the plain-load kernel, the three
-# decode kernels, C = act(beta*C + bias) without the product, and both TF32
-# tensor-core kernels.
-EPI_CASES = [  # (M, N, K, kernel, tensor_cores, ldb padding)
-    (300, 260, 516, TMA, False, 0),        # 9 tiles, split along K
-    (1100, 700, 200, TMA, False, 0),       # whole tiles
-    (150, 130, 70, GEN, False, 3),
-    (16, 1000, 512, DEC, False, 0),        # outer-product decode kernel
-    (4, 1000, 700, DEC, False, 0),         # TMA decode kernel
-    (8, 999, 700, DEC, False, 3),          # direct-load decode kernel (B unaligned)
-    (256, 384, 200, sg.KERNEL_TF32X3, True, 0),
-    (256, 384, 200, sg.KERNEL_TF32, sg.MODE_TF32, 0),
-    (256, 384, 200, sg.KERNEL_BF16, sg.MODE_BF16, 0),
+# kernel (whole tiles and a split last wave), the plain-load kernel, the
+# decode kernels (both outer-product tiles, the TMA and the direct-load
+# kernel), C = act(beta*C + bias) without the product, and the tensor-core
+# kernels on one-SM and two-SM tiles in all three arithmetics.
+EPI_CASES = [  # (M, N, K, kernel, tensor_cores, ldb padding, lda padding)
+    (300, 260, 516, TMA, False, 0, 0),        # 9 tiles, split along K
+    (1100, 700, 200, TMA, False, 0, 0),       # whole tiles
+    (150, 130, 70, GEN, False, 3, 0),
+    (16, 1000, 512, DEC, False, 0, 0),        # outer-product decode kernel, 16-row tile
+    (4, 1000, 700, DEC, False, 0, 0),         # outer-product decode kernel, 8-row tile
+    (4, 1000, 700, DEC, False, 0, 1),         # TMA decode kernel (A unaligned)
+    (8, 999, 700, DEC, False, 3, 0),          # direct-load decode kernel (B unaligned)
+    (256, 384, 200, sg.KERNEL_TF32X3, True, 0, 0),           # two-SM tensor-core tiles
+    (256, 384, 200, sg.KERNEL_TF32, sg.MODE_TF32, 0, 0),
+    (256, 384, 200, sg.KERNEL_BF16, sg.MODE_BF16, 0, 0),
+    (200, 384, 200, sg.KERNEL_TF32X3, True, 0, 0),           # one-SM tensor-core tiles
+    (200, 384, 200, sg.KERNEL_TF32, sg.MODE_TF32, 0, 0),
+    (200, 384, 200, sg.KERNEL_BF16, sg.MODE_BF16, 0, 0),
 ]
 
 
 @pytest.mark.parametrize("act", ["none", "relu", "gelu", "silu"])
-@pytest.mark.parametrize("M,N,K,kern,tc,pad", EPI_CASES)
-def test_fused_epilogue(M, N, K, kern, tc, pad, act):
+@pytest.mark.parametrize("M,N,K,kern,tc,pad,apad", EPI_CASES)
+def test_fused_epilogue(M, N, K, kern, tc, pad, apad, act):
     A, B, C0 = make_inputs(M, N, K, "normal", seed=M + N + K, beta=0.5)
     bias = synth.matrix(1, N, seed=M + K, stream=3, dist="normal")[0] * 4
-    lds = (K, N + pad, N + 1) if pad else (None, None, None)
+    lds = (K + apad, N + pad, N + 1) if (pad or apad) else (None, None, None)
     _, chosen = run_checked(sg, A, B, C0, 0.1, 0.5, tensor_cores=tc, bias=bias, act=act, lds=lds)
     assert chosen == kern
 
