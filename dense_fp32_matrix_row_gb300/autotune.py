@@ -211,7 +211,7 @@ print("RESULT", json.dumps({{f"{{M}}x{{N}}x{{K}}": autotune._time(sg, torch, M, 
 """
 
 
-def run_search(workdir: str, shapes: list[tuple[int, int, int]], tiles) -> None:
+def run_search(workdir: str, shapes: list[tuple[int, int, int]], tiles, only: str = "") -> None:
     # the package re-exports the build() function under the module's name,
     # so import the function itself
     from .build import build as build_library
@@ -219,6 +219,8 @@ def run_search(workdir: str, shapes: list[tuple[int, int, int]], tiles) -> None:
     results = {}
     for cand in candidates(tiles):
         name = "tm{}_tn{}_wm{}_wn{}_bk{}_st{}_mb{}".format(*cand)
+        if only and not any(o in name for o in only.split(",")):
+            continue
         flags = [f"-DFFMA_{k}={v}" for k, v in zip(("TM", "TN", "WM", "WN", "BK", "STAGES", "MINB"), cand)]
         lib = os.path.join(workdir, name, "libsgemm_gb300.so")
         try:
@@ -254,6 +256,8 @@ def main(argv=None) -> int:
     s.add_argument("--shapes", default="4092x4092x4092,8192x8192x8192,1024x1024x1024",
                    help="comma-separated MxNxK")
     s.add_argument("--tiles", default="8x8", help="thread tiles TMxTN to search, comma-separated")
+    s.add_argument("--only", default="",
+                   help="comma-separated name fragments; only candidates whose name contains one run")
     args = ap.parse_args(argv)
     if args.cmd == "table":
         if args.from_report:
@@ -264,7 +268,7 @@ def main(argv=None) -> int:
     else:
         shapes = [tuple(int(v) for v in s.split("x")) for s in args.shapes.split(",")]
         tiles = tuple(tuple(int(v) for v in t.split("x")) for t in args.tiles.split(","))
-        run_search(args.workdir, shapes, tiles)
+        run_search(args.workdir, shapes, tiles, args.only)
     return 0
 
 
