@@ -190,6 +190,48 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// One epilogue thread's row of a tile: C[gm][gn0 .. gn0 + EPI_COLS) =
+// act(alpha*acc + beta*C + bias), C read only when beta != 0; rows past M
+// and columns past N are skipped.
+__device__ __forceinline__ void store_row(const float (&acc)[EPI_COLS], const Epilogue &ep,
+                                          float *__restrict__ C, int64_t ldc, int gm, int gn0,
+                                          int M, int N, int c_vec4) {
+    if (gm >= M) return;
+    const bool tail = ep.bias != nullptr || ep.act != kActNone;
+    float *crow = C + (int64_t)gm * ldc;
+#pragma unroll
+    for (int q = 0; q < EPI_COLS / 4; ++q) {
+        const int gn = gn0 + 4 * q;
+        float o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = ep.alpha * acc[4 * q + e];
+        if (c_vec4 && gn + 3 < N) {
+            float4 *p = reinterpret_cast<float4 *>(crow + gn);
+            if (ep.beta != 0.0f) {
+                const float4 cv = *p;
+                o[0] = fmaf(ep.beta, cv.x, o[0]);
+                o[1] = fmaf(ep.beta, cv.y, o[1]);
+                o[2] = fmaf(ep.beta, cv.z, o[2]);
+                o[3] = fmaf(ep.beta, cv.w, o[3]);
+            }
+            if (tail) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = epilogue_tail(ep, o[e], gn + e);
+            }
+            *p = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (gn + e < N) {
+                    float *p = crow + gn + e;
+                    const float w = (ep.beta != 0.0f) ? fmaf(ep.beta, *p, o[e]) : o[e];
+                    *p = tail ? epilogue_tail(ep, w, gn + e) : w;
+                }
+            }
+        }
+    }
+}
+
 // Chunked accumulation.  A tensor-core MMA adds its products into the FP32
 // accumulator with an error of a fraction of an ulp of the accumulator, so a
 // single accumulator over all of K loses accuracy linearly in K (measured:
@@ -365,7 +407,6 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
         // while the MMAs of the next tile fill the other accumulator buffer.
         const int lane_base = (warp & 3) * 32;
         const int col_base = (warp >> 2) * EPI_COLS;
-        const bool tail = ep.bias != nullptr || ep.act != kActNone;
         bool ok = true;
         uint32_t gc = 0;   // chunks drained, over all tiles
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
@@ -403,40 +444,7 @@ tf32_mma_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant
             }
             if (!ok) break;
             const int gm = m0 + lane_base + lane;
-            if (gm < M) {
-                float *crow = C + (int64_t)gm * ldc;
-#pragma unroll
-                for (int q = 0; q < EPI_COLS / 4; ++q) {
-                    const int gn = n0 + col_base + 4 * q;
-                    float o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e] = ep.alpha * acc[4 * q + e];
-                    if (c_vec4 && gn + 3 < N) {
-                        float4 *p = reinterpret_cast<float4 *>(crow + gn);
-                        if (ep.beta != 0.0f) {
-                            const float4 cv = *p;
-                            o[0] = fmaf(ep.beta, cv.x, o[0]);
-                            o[1] = fmaf(ep.beta, cv.y, o[1]);
-                            o[2] = fmaf(ep.beta, cv.z, o[2]);
-                            o[3] = fmaf(ep.beta, cv.w, o[3]);
-                        }
-                        if (tail) {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) o[e] = epilogue_tail(ep, o[e], gn + e);
-                        }
-                        *p = make_float4(o[0], o[1], o[2], o[3]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (gn + e < N) {
-                                float *p = crow + gn + e;
-                                const float w = (ep.beta != 0.0f) ? fmaf(ep.beta, *p, o[e]) : o[e];
-                                *p = tail ? epilogue_tail(ep, w, gn + e) : w;
-                            }
-                        }
-                    }
-                }
-            }
+            store_row(acc, ep, C, ldc, gm, n0 + col_base, M, N, c_vec4);
         }
         if (!ok && lane == 0) record_error(err, kErrWaitTimeout);
     }
@@ -759,7 +767,6 @@ tf32_mma2_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constan
         // CTA's tensor-memory lanes), columns (w / 4) * EPI_COLS .. + EPI_COLS.
         const int lane_base = (warp & 3) * 32;
         const int col_base = (warp >> 2) * EPI_COLS;
-        const bool tail = ep.bias != nullptr || ep.act != kActNone;
         bool ok = true;
         uint32_t gc = 0;
         for (int t = pair; t < tiles && ok; t += npairs) {
@@ -795,40 +802,7 @@ tf32_mma2_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constan
             }
             if (!ok) break;
             const int gm = m0 + TBM * (int)rank + lane_base + lane;
-            if (gm < M) {
-                float *crow = C + (int64_t)gm * ldc;
-#pragma unroll
-                for (int q = 0; q < EPI_COLS / 4; ++q) {
-                    const int gn = n0 + col_base + 4 * q;
-                    float o[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e] = ep.alpha * acc[4 * q + e];
-                    if (c_vec4 && gn + 3 < N) {
-                        float4 *p = reinterpret_cast<float4 *>(crow + gn);
-                        if (ep.beta != 0.0f) {
-                            const float4 cv = *p;
-                            o[0] = fmaf(ep.beta, cv.x, o[0]);
-                            o[1] = fmaf(ep.beta, cv.y, o[1]);
-                            o[2] = fmaf(ep.beta, cv.z, o[2]);
-                            o[3] = fmaf(ep.beta, cv.w, o[3]);
-                        }
-                        if (tail) {
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) o[e] = epilogue_tail(ep, o[e], gn + e);
-                        }
-                        *p = make_float4(o[0], o[1], o[2], o[3]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (gn + e < N) {
-                                float *p = crow + gn + e;
-                                const float w = (ep.beta != 0.0f) ? fmaf(ep.beta, *p, o[e]) : o[e];
-                                *p = tail ? epilogue_tail(ep, w, gn + e) : w;
-                            }
-                        }
-                    }
-                }
-            }
+            store_row(acc, ep, C, ldc, gm, n0 + col_base, M, N, c_vec4);
         }
         if (!ok && lane == 0) record_error(err, kErrWaitTimeout);
     }
