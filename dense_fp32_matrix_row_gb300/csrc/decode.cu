@@ -615,8 +615,15 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
         if constexpr (L::TRANSPOSE_A) __syncwarp();   // lanes are done with `at` before it is rewritten
         __syncwarp();
         if (lane == 0) {
-            __threadfence_block();
-            if (atomicAdd(&arrived[s], 1u) == DO_WARPS - 1) {
+            // release: this warp's reads of the stage happen before its arrival;
+            // acquire: the last warp to arrive sees every other warp's release
+            // before it lets the copy engine overwrite the stage
+            unsigned prev;
+            asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                         : "=r"(prev)
+                         : "r"(smem_u32(&arrived[s]))
+                         : "memory");
+            if (prev == DO_WARPS - 1) {
                 arrived[s] = 0;
                 if (st + DO_STAGES < nst) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
