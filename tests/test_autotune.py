@@ -115,3 +115,37 @@ def test_pick_keeps_the_default_within_the_margin():
     assert autotune.pick([60.0, 60.2, 59.0]) == 0          # 0.3% is noise
     assert autotune.pick([60.0, 61.0, 59.0]) == 1
     assert autotune.pick([10.0, 9.0, 9.5]) == 0
+
+
+def test_search_runs_only_the_named_candidates(monkeypatch, tmp_path, capsys):
+    # the search builds and times a variant library per candidate; here the
+    # build and the timing child are stand-ins, so only the selection and
+    # the report are exercised
+    import json as _json
+    import importlib
+    build_mod = importlib.import_module("dense_fp32_matrix_row_gb300.build")
+    built = []
+
+    def fake_build(extra_flags=None, library=None, **kw):
+        built.append((tuple(extra_flags), library))
+        return library
+
+    class Done:
+        def __init__(self, out):
+            self.returncode, self.stdout, self.stderr = 0, out, ""
+
+    def fake_run(cmd, capture_output, text, timeout):
+        tflops = 60.0 + len(built)   # later candidates "measure" faster
+        return Done("RESULT " + _json.dumps({"4092x4092x4092": tflops}) + "\n")
+
+    monkeypatch.setattr(build_mod, "build", fake_build)
+    monkeypatch.setattr(autotune.subprocess, "run", fake_run)
+    autotune.run_search(str(tmp_path), [(4092, 4092, 4092)], ((8, 8),),
+                        only="wm2_wn2_bk32_st2_mb4,wm4_wn1_bk32_st2_mb4")
+    names = [os.path.basename(os.path.dirname(lib)) for _, lib in built]
+    assert names == ["tm8_tn8_wm2_wn2_bk32_st2_mb4", "tm8_tn8_wm4_wn1_bk32_st2_mb4"]
+    assert all("-DFFMA_MINB=4" in flags for flags, _ in built)
+    out = capsys.readouterr().out
+    assert "best tm8_tn8_wm4_wn1_bk32_st2_mb4" in out
+    with pytest.raises(RuntimeError):
+        autotune.run_search(str(tmp_path), [(4092, 4092, 4092)], ((8, 8),), only="no_such_name")
