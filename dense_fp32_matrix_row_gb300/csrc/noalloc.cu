@@ -2,8 +2,10 @@
 // not allocate device memory (see include/sgemm_gb300.h).  The FFMA kernel's
 // transposed copy of A lives in a fixed file-scope __device__ array instead
 // of the per-stream workspace that sgemm() grows with cudaMallocAsync.  The
-// array sits in its own translation unit, so its module -- and its 64 MiB --
-// is loaded on a device only once this entry point runs there.
+// array sits in its own translation unit, so under lazy module loading (the
+// CUDA default) its module -- and its 64 MiB -- is loaded on a device only
+// once this entry point runs there; with CUDA_MODULE_LOADING=EAGER it is
+// resident on every device the process initialises, from context creation.
 #include <mutex>
 
 #include "common.cuh"
@@ -48,10 +50,19 @@ extern "C" int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha, const
                              int64_t ldc, void *stream) {
     const int kid = sgemm_select_kernel(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 0);
     if (kid < 0) return kid;
-    // Only the FFMA tile kernel uses scratch; every other choice allocates
-    // nothing and runs through sgemm() unchanged.
-    if (kid != SGEMM_KERNEL_FFMA_TMA)
-        return sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+    // Only the FFMA tile kernel uses scratch.  The kernels that need none run
+    // through sgemm() unchanged.  The tensor-core kernels need a workspace and
+    // can be chosen here only when forced with sgemm_force_kernel; they are
+    // refused rather than handed to sgemm(), which would allocate one.
+    switch (kid) {
+        case SGEMM_KERNEL_NONE:
+        case SGEMM_KERNEL_SCALE_C:
+        case SGEMM_KERNEL_DECODE:
+        case SGEMM_KERNEL_FFMA_GENERIC:
+            return sgemm(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream);
+        case SGEMM_KERNEL_FFMA_TMA: break;
+        default: return SGEMM_ERR_BAD_ARG;
+    }
     if (K > kScratchFloats / ffma_tma_at_ld(M)) return SGEMM_ERR_TOO_LARGE;
     float *scratch = nullptr;
     int rc = scratch_address(&scratch);

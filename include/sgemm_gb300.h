@@ -341,6 +341,8 @@ int sgemm_release_workspaces(void);
  * aligned, ldb % 4 == 0) need K * round_up(M, 4) <= 16,777,216 floats
  * (M = K = 4096 just fits); larger ones return SGEMM_ERR_TOO_LARGE with
  * nothing enqueued.  All other shapes use no scratch and run as in sgemm().
+ * A tensor-core kernel forced with sgemm_force_kernel (a test hook) needs a
+ * workspace, so such a call returns SGEMM_ERR_BAD_ARG with nothing enqueued.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current).  Make that first call
  * before any stream capture.
@@ -350,7 +352,10 @@ int sgemm_release_workspaces(void);
  * different streams, or from host threads that do not order their streams)
  * race on the array: run them on one stream or serialise them.
  * The array occupies 64 MiB on each GPU where this entry point has been used,
- * until the process exits.
+ * until the process exits.  That holds under lazy module loading, the CUDA
+ * default; with CUDA_MODULE_LOADING=EAGER the array is resident on every
+ * device the process initialises, from context creation, whether or not
+ * this entry point is ever called.
  * Arguments, conventions and other errors are those of sgemm().
  */
 int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,

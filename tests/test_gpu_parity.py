@@ -227,10 +227,7 @@ def test_bounded_wait_times_out_and_context_survives():
 
 
 # ---------------------------------------------------------------- full-size workloads
-def _sample_rows(M, stride=61):
-    return np.unique(np.r_[np.arange(0, M, stride), [M - 1]])
-
-
+# (the 4092^3 integer case, 8192^3 and the prefill GEMMs: test_gpu_full_size.py)
 @pytest.mark.parametrize("name", ["sgemm_128", "sgemm_128_int", "decode_m1", "decode_m4",
                                   "decode_m16"])
 def test_workload_full(name):
@@ -245,19 +242,6 @@ def test_workload_4092_full():
     A, B, C0, w = synth.workload_inputs("sgemm_4092")
     err, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"])
     assert chosen == TMA and err <= GATE
-
-
-def test_workload_4092_int_exact():
-    A, B, C0 = make_inputs(4092, 4092, 4092, "int", seed=1, beta=0.5)
-    run_checked(sg, A, B, C0, 1.0, 0.5, exact=True, rows=_sample_rows(4092, 31))
-
-
-@pytest.mark.parametrize("name", ["sgemm_8192", "prefill_qkv", "prefill_up", "prefill_down"])
-def test_workload_large_sampled_rows(name):
-    """Sampled rows (stride 61 < the 128-row tile, so every tile band is hit)."""
-    A, B, C0, w = synth.workload_inputs(name)
-    C0 = np.full((w["M"], w["N"]), np.nan, np.float32) if C0 is None else C0
-    run_checked(sg, A, B, C0, w["alpha"], w["beta"], rows=_sample_rows(w["M"]))
 
 
 # ---------------------------------------------------------------- 3xTF32 tensor-core path
@@ -498,14 +482,6 @@ def test_tf32_is_one_term():
     assert err_exact > 3 * GATE, err_exact
 
 
-def test_workload_8192_tf32_sampled_rows():
-    A, B, C0, w = synth.workload_inputs("sgemm_8192")
-    C0 = np.full((w["M"], w["N"]), np.nan, np.float32)
-    _, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"], tensor_cores=sg.MODE_TF32,
-                            rows=_sample_rows(w["M"]))
-    assert chosen == TF1
-
-
 # ---------------------------------------------------------------- BF16 (sgemm_bf16)
 # The contract: A and B rounded to BF16 (nearest, ties to even), then the FP32
 # product -- checked against the oracle on rounded operands at the FP32 gate.
@@ -567,22 +543,6 @@ def test_bf16_is_bf16():
     assert normwise_err(got, oracle.sgemm(A, B, inputs="bf16"), A, B, K) <= GATE
     assert normwise_err(got, oracle.sgemm(A, B), A, B, K) > 30 * GATE
     assert normwise_err(got, oracle.sgemm(A, B, inputs="tf32"), A, B, K) > 30 * GATE
-
-
-def test_workload_8192_bf16_sampled_rows():
-    A, B, C0, w = synth.workload_inputs("sgemm_8192")
-    C0 = np.full((w["M"], w["N"]), np.nan, np.float32)
-    _, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"], tensor_cores=sg.MODE_BF16,
-                            rows=_sample_rows(w["M"]))
-    assert chosen == BF
-
-
-def test_workload_8192_3xtf32_sampled_rows():
-    A, B, C0, w = synth.workload_inputs("sgemm_8192")
-    C0 = np.full((w["M"], w["N"]), np.nan, np.float32)
-    _, chosen = run_checked(sg, A, B, C0, w["alpha"], w["beta"], tensor_cores=True,
-                            rows=_sample_rows(w["M"]))
-    assert chosen == TF
 
 
 # ---------------------------------------------------------------- large ragged shapes

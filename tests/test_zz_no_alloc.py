@@ -5,10 +5,22 @@ their device memory is all reserved up front by their own pool or by a host
 framework, or the call sits on a latency-critical path.  sgemm_noalloc keeps
 the FFMA kernel's transposed copy of A in a fixed array compiled into the
 library instead of a workspace it allocates.  These tests call it through the
-C ABI and check it against sgemm() -- the entry point that does allocate --
-within the parity gate, on two calls in a row (the second call reuses the
-array the first one left behind), and check that oversized problems are
-refused.  The file is named to be collected last.
+C ABI and check:
+
+  - its output against the fp64 oracle (the parity gate) and against sgemm(),
+    the entry point that does allocate, on two calls in a row (the second
+    call reuses the array the first one left behind);
+  - a problem that fills the array exactly, with a partial last wave: there
+    is no room for the split last wave's partial tiles, so the last wave runs
+    unsplit (a different summation order from sgemm()'s) and still meets the
+    gate;
+  - that a call allocates nothing: with every sgemm() workspace released,
+    device free memory does not drop across a call, while the same call
+    through sgemm() then takes memory for its workspace;
+  - that a tensor-core kernel forced with the test hook is refused, and that
+    problems beyond the array are refused before any launch.
+
+The file is named to be collected last.
 """
 
 import ctypes
@@ -16,6 +28,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import synth
 from gpu_util import GATE, normwise_err
 
@@ -29,50 +42,150 @@ import dense_fp32_matrix_row_gb300 as sg  # noqa: E402
 
 _i64, _f32, _vp = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
 SGEMM_ERR_TOO_LARGE = -9
+ARRAY_FLOATS = 1 << 24          # the fixed array: 16,777,216 floats
 
 
 @pytest.fixture(scope="module")
 def noalloc():
     sg.build()
+    sg.force_kernel(sg.KERNEL_AUTO)
     fn = sg.lib().sgemm_noalloc
     fn.argtypes = [_i64, _i64, _i64, _f32, _vp, _i64, _vp, _i64, _f32, _vp, _i64, _vp]
     fn.restype = ctypes.c_int
     return fn
 
 
-def _compare_one(noalloc, M, N, K, alpha, beta, seed):
+def _operands(M, N, K, seed):
     A = synth.matrix(M, K, seed=seed, stream=0, dist="normal")
     B = synth.matrix(K, N, seed=seed, stream=1, dist="normal")
     C0 = synth.matrix(M, N, seed=seed, stream=2, dist="normal")
+    return A, B, C0
+
+
+def _call(noalloc, dA, dB, dC, alpha, beta, stream=None):
+    M, K = dA.shape
+    N = dB.shape[1]
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    return noalloc(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta, dC.data_ptr(), N, s)
+
+
+def _compare_one(noalloc, M, N, K, alpha, beta, seed):
+    """One sgemm_noalloc call against the oracle and against sgemm()."""
+    A, B, C0 = _operands(M, N, K, seed)
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     want = torch.from_numpy(C0).cuda()
     got = want.clone()
     kid = sg.select_kernel(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta,
                            got.data_ptr(), N)
     assert kid == sg.KERNEL_FFMA_TMA, "these shapes must take the scratch-using kernel"
-    stream = torch.cuda.current_stream().cuda_stream
-    sg.sgemm(dA, dB, want, alpha, beta)
-    rc = noalloc(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta, got.data_ptr(), N,
-                 stream)
+    rc = _call(noalloc, dA, dB, got, alpha, beta)
     assert rc == sg.OK, sg.status_string(rc)
     assert sg.status() == sg.OK
-    err = normwise_err(got.cpu().numpy(), want.cpu().numpy(), A, B, K, alpha, beta, C0)
+    sg.sgemm(dA, dB, want, alpha, beta)
+    assert sg.status() == sg.OK
+    got_h, want_h = got.cpu().numpy(), want.cpu().numpy()
+    ref = oracle.sgemm(A, B, C0, alpha=alpha, beta=beta)
+    err = normwise_err(got_h, ref, A, B, K, alpha, beta, C0)
+    assert err <= GATE, f"sgemm_noalloc against the oracle: {err:.3e}"
+    err = normwise_err(got_h, want_h, A, B, K, alpha, beta, C0)
     assert err <= GATE, f"sgemm_noalloc differs from sgemm: {err:.3e}"
+    return got_h, want_h
 
 
-def test_matches_sgemm_on_two_calls_in_a_row(noalloc):
+def test_matches_oracle_and_sgemm_on_two_calls_in_a_row(noalloc):
     # The first call fills more of the array than the second reads.
     _compare_one(noalloc, 1000, 700, 1500, 1.0, 0.5, seed=41)
     _compare_one(noalloc, 300, 516, 260, -0.75, 0.0, seed=42)
 
 
+def _split_expected(M, N, K, at_floats, capacity):
+    """Whether the FFMA kernel's last wave is split along K for this shape
+    when `capacity` floats of scratch are available (the library's rule: the
+    tiles after the last full wave of resident CTAs fill at most half a wave,
+    each of at least 2 parts keeps 4 k-tiles, and 1024 counters plus one
+    BM x BN partial tile per part fit beside A^T)."""
+    cfg = sg.ffma_configs()[sg.ffma_config_for(M, N)]
+    bm, bn, bk = cfg["bm"], cfg["bn"], cfg["bk"]
+    slots = cfg["ctas_per_sm"] * torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-M // bm) * -(-N // bn)
+    rem = tiles % slots
+    if rem == 0 or 2 * rem > slots or rem > 1024:
+        return False
+    if min(slots // rem, 16, -(-K // bk) // 4) < 2:
+        return False
+    return at_floats + 1024 + rem * 2 * bm * bn <= capacity
+
+
+def test_full_array_runs_the_last_wave_unsplit(noalloc):
+    # M = K = 4096: A^T fills the array, so the partial tiles of a split last
+    # wave have no room.  N is picked so that the last wave is partial and
+    # sgemm() (whose workspace grows) does split it.
+    M = K = 4096
+    at = K * M
+    assert at == ARRAY_FLOATS
+    N = next(n for n in (512, 384, 640, 256, 768, 896, 1152)
+             if _split_expected(M, n, K, at, 1 << 40))
+    assert not _split_expected(M, N, K, at, ARRAY_FLOATS)
+    got, want = _compare_one(noalloc, M, N, K, 1.0, 0.25, seed=43)
+    # the two entry points summed the last wave's tiles in different orders
+    assert not np.array_equal(got, want)
+
+
+def test_allocates_nothing(noalloc):
+    M, N, K = 1000, 700, 1500
+    A, B, C0 = _operands(M, N, K, seed=44)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda()
+    # set-up call (module load, array address)
+    assert _call(noalloc, dA, dB, dC, 1.0, 0.0) == sg.OK
+    stream = torch.cuda.Stream()
+    # no workspace anywhere: an sgemm()-style call would have to allocate one
+    assert sg.release_workspaces() == sg.OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    assert _call(noalloc, dA, dB, dC, 1.0, 0.0, stream=stream) == sg.OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 >= free0, f"sgemm_noalloc took {free0 - free1} bytes of device memory"
+    got = dC.cpu().numpy()
+    # the same measurement sees sgemm()'s workspace (4 * K * M bytes of A^T)
+    rc = sg.lib().sgemm(M, N, K, 1.0, dA.data_ptr(), K, dB.data_ptr(), N, 0.0, dC.data_ptr(), N,
+                        stream.cuda_stream)
+    assert rc == sg.OK
+    torch.cuda.synchronize()
+    free2, _ = torch.cuda.mem_get_info()
+    assert free1 - free2 >= 4 * K * M, "the free-memory measurement did not see sgemm()'s workspace"
+    assert sg.status() == sg.OK
+    ref = oracle.sgemm(A, B, alpha=1.0, beta=0.0)
+    assert normwise_err(got, ref, A, B, K) <= GATE
+
+
+@pytest.mark.parametrize("forced", [sg.KERNEL_TF32X3, sg.KERNEL_TF32, sg.KERNEL_BF16])
+def test_forced_tensor_core_kernel_is_refused(noalloc, forced):
+    M, N, K = 300, 256, 260
+    A, B, C0 = _operands(M, N, K, seed=45)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.from_numpy(C0).cuda()
+    prev = sg.force_kernel(forced)
+    try:
+        rc = _call(noalloc, dA, dB, dC, 1.0, 0.5)
+    finally:
+        sg.force_kernel(prev)
+    assert rc == sg.ERR_BAD_ARG
+    torch.cuda.synchronize()
+    assert np.array_equal(dC.cpu().numpy(), C0), "a refused call changed C"
+
+
 def test_refuses_problems_beyond_the_array(noalloc):
     # K * round_up(M, 4) = 4100 * 4100 > 16,777,216: refused before any
-    # launch, so the (never dereferenced) pointers need only be distinct.
-    a, b, c = 1 << 30, 1 << 31, 3 << 30
+    # launch.  Real device buffers, so a regression gives a wrong result
+    # rather than a bad address.
     M = N = K = 4100
-    rc = noalloc(M, N, K, 1.0, a, K, b, N, 0.0, c, N, 0)
-    assert rc == SGEMM_ERR_TOO_LARGE
-    assert "fixed scratch" in sg.status_string(rc)
-    # M = K = 4096 exactly fills the array and is accepted by the size check.
-    assert sg.select_kernel(4096, 64, 4096, 1.0, a, 4096, b, 64, 0.0, c, 64) == sg.KERNEL_FFMA_TMA
+    dA = torch.zeros((M, K), device="cuda")
+    dB = torch.zeros((K, N), device="cuda")
+    dC = torch.full((M, N), 3.0, device="cuda")
+    assert _call(noalloc, dA, dB, dC, 1.0, 0.0) == SGEMM_ERR_TOO_LARGE
+    assert "fixed scratch" in sg.status_string(SGEMM_ERR_TOO_LARGE)
+    torch.cuda.synchronize()
+    assert bool((dC == 3.0).all()), "a refused call changed C"
+    assert sg.status() == sg.OK
