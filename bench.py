@@ -326,30 +326,47 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
     "ms_eager" per call with an event pair around each eager call."""
     import synth
     out = {}
+    # measured bf16 x the nominal TF32 / BF16 ratio, burst and sustained
+    tf32_peak = peaks["bf16_tflops"] * 1.1 / 2.25
+    tf32_peak_s = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1.1 / 2.25
     tf32_peak = peaks["bf16_tflops"] * 1.1 / 2.25   # measured bf16 x nominal tf32/bf16
 
-    def graph_ms(fns):
-        """Mean ms per call of the calls `fns` captured in one CUDA graph."""
+    def capture(fns):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for f in fns:
                 f()
+        return graph
+
+    def replay_ms(graph, n):
+        """ms per call of one replay of a graph of n calls."""
         with torch.cuda.stream(stream):
-            graph.replay()                      # warm replay
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             graph.replay()
             e1.record(stream)
         torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def graph_ms(fns):
+        """Mean ms per call of the calls `fns` captured in one CUDA graph
+        (after one warm replay)."""
+        graph = capture(fns)
+        replay_ms(graph, len(fns))
+        ms = replay_ms(graph, len(fns))
         del graph
-        return e0.elapsed_time(e1) / len(fns)
+        return ms
 
     def bench_shape(A, B, C0, alpha, beta, mode=sg.MODE_FP32, activation="none", rotate=1,
-                    inputs="fp32", bias_seed=None):
+                    inputs="fp32", bias_seed=None, burst=False):
         """Parity of the first call, then timing.  With rotate > 1 the calls
         cycle through that many copies of B (distinct device buffers), so no
-        call finds its B in L2 from the call before."""
+        call finds its B in L2 from the call before.  With `burst` (the
+        tensor-core lines, whose speed depends on how long the GPU has been
+        under load): "ms" is the graph replayed after a second of idling,
+        "ms_sustained" the graph replayed again after about a second of
+        back-to-back calls, and "ms_eager" follows, still under load."""
         M, K = A.shape
         N = B.shape[1]
         dA = torch.from_numpy(A).to(dev)
@@ -381,6 +398,16 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
             with torch.cuda.stream(stream):
                 fns[i % rotate]()
         torch.cuda.synchronize()
+        if burst:
+            graph = capture([fns[i % rotate] for i in range(steps)])
+            replay_ms(graph, steps)            # warm replay
+            time.sleep(1.0)
+            res["ms"] = replay_ms(graph, steps)
+            t_end = time.time() + 1.0
+            while time.time() < t_end:
+                replay_ms(graph, steps)
+            res["ms_sustained"] = replay_ms(graph, steps)
+            del graph
         evs = []
         with torch.cuda.stream(stream):
             for i in range(steps):
@@ -391,7 +418,8 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
                 evs.append(e)
         torch.cuda.synchronize()
         res["ms_eager"] = float(np.mean([a.elapsed_time(b) for a, b in evs]))
-        res["ms"] = graph_ms([fns[i % rotate] for i in range(steps)])
+        if not burst:
+            res["ms"] = graph_ms([fns[i % rotate] for i in range(steps)])
         if rotate > 1:
             res["ms_same_buffer"] = graph_ms([fns[0]] * steps)
             res["b_buffers"] = rotate
@@ -429,6 +457,31 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
         out[f"decode_m{M}"] = r
         del A, B
 
+    # skinny products, 17 <= M <= 128 rows on the decode shapes' N and K (the
+    # same B): HBM-bound below about 24 rows, FFMA-bound above
+    ffma_peak = None
+    for M in (32, 64, 128):
+        A, B, _, w = synth.workload_inputs("decode_m16")
+        A = synth.matrix(M, w["K"], seed=w["seed"], stream=0, dist="normal")
+        N, K = w["N"], w["K"]
+        r = bench_shape(A, B, None, 1.0, 0.0, rotate=3)
+        nbytes = 4 * (M * K + K * N + M * N)
+        if ffma_peak is None:
+            props = torch.cuda.get_device_properties(dev)
+            ffma_peak = props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+        t_alu = 2.0 * M * N * K / (ffma_peak * 1e12) * 1e3
+        r["TFLOP/s"] = tflops(r, M, N, K)
+        r["GB/s"] = nbytes / (r["ms"] * 1e-3) / 1e9
+        r["bound"] = "alu" if t_alu >= t_hbm else "hbm"
+        r["frac_bound"] = max(t_alu, t_hbm) / r["ms"]
+        r["frac_ffma_peak"] = r["TFLOP/s"] / ffma_peak
+        r["frac_hbm"] = r["GB/s"] / peaks["hbm_gbs"]
+        r["data"] = "A normal(0,1) seed 3, B the decode workloads' B (normal(0,0.02), seed 3)"
+        r["l2"] = "B rotates through 3 buffers (705 MB > 129 MB L2)"
+        out[f"skinny_m{M}"] = r
+        del A, B
+
     # the compute-bound workloads on the FFMA path
     for name in ("sgemm_8192", "prefill_qkv", "prefill_up", "prefill_down"):
         A, B, C0, w = synth.workload_inputs(name)
@@ -443,23 +496,33 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
             r["epilogue"] = "bias + SiLU (sgemm_fused)"
             out["prefill_up_bias_silu"] = r
         if name == "sgemm_8192":
-            # the tensor-core paths on the same operands
-            r = bench_shape(A, B, C0, w["alpha"], w["beta"], mode=sg.MODE_3XTF32)
-            useful = tflops(r, M, N, K)
+            # the tensor-core paths on the same operands: burst (after idling)
+            # against the burst peak, sustained against the sustained peak
+            r = bench_shape(A, B, C0, w["alpha"], w["beta"], mode=sg.MODE_3XTF32, burst=True)
+            useful, useful_s = tflops(r, M, N, K), tflops(r, M, N, K, "ms_sustained")
             r.update({"TFLOP/s": useful, "tensor_TFLOP/s": 3 * useful, "tf32_peak": tf32_peak,
                       "frac_tf32_peak": 3 * useful / tf32_peak,
                       "frac_useful_ceiling": useful / (tf32_peak / 3),
+                      "TFLOP/s_sustained": useful_s, "tf32_peak_sustained": tf32_peak_s,
+                      "frac_tf32_peak_sustained": 3 * useful_s / tf32_peak_s,
                       "TFLOP/s_eager": tflops(r, M, N, K, "ms_eager")})
             out["sgemm_8192_3xtf32"] = r
-            r = bench_shape(A, B, C0, w["alpha"], w["beta"], mode=sg.MODE_TF32, inputs="tf32")
-            t = tflops(r, M, N, K)
+            r = bench_shape(A, B, C0, w["alpha"], w["beta"], mode=sg.MODE_TF32, inputs="tf32",
+                            burst=True)
+            t, ts = tflops(r, M, N, K), tflops(r, M, N, K, "ms_sustained")
             r.update({"TFLOP/s": t, "tf32_peak": tf32_peak, "frac_tf32_peak": t / tf32_peak,
+                      "TFLOP/s_sustained": ts, "tf32_peak_sustained": tf32_peak_s,
+                      "frac_tf32_peak_sustained": ts / tf32_peak_s,
                       "TFLOP/s_eager": tflops(r, M, N, K, "ms_eager")})
             out["sgemm_8192_tf32"] = r
-            r = bench_shape(A, B, C0, w["alpha"], w["beta"], mode=sg.MODE_BF16, inputs="bf16")
-            t = tflops(r, M, N, K)
+            r = bench_shape(A, B, C0, w["alpha"], w["beta"], mode=sg.MODE_BF16, inputs="bf16",
+                            burst=True)
+            t, ts = tflops(r, M, N, K), tflops(r, M, N, K, "ms_sustained")
+            bf_s = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
             r.update({"TFLOP/s": t, "bf16_peak": peaks["bf16_tflops"],
                       "frac_bf16_peak": t / peaks["bf16_tflops"],
+                      "TFLOP/s_sustained": ts, "bf16_peak_sustained": bf_s,
+                      "frac_bf16_peak_sustained": ts / bf_s,
                       "TFLOP/s_eager": tflops(r, M, N, K, "ms_eager")})
             out["sgemm_8192_bf16"] = r
         del A, B

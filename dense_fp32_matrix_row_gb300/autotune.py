@@ -39,7 +39,7 @@ TMA_BOX_MAX = 256                  # elements per box dimension
 
 # M and N class upper bounds of the table (the last class is unbounded), the
 # fractions of the bound at which each class is measured, and the depths
-M_CLASSES = [64, 128, 256, 512, 1024, 2048, 4096, 8192]
+M_CLASSES = [32, 64, 128, 256, 512, 1024, 2048, 4096, 8192]
 N_CLASSES = [256, 512, 1024, 2048, 4096, 8192]
 POINTS = [1.0, 0.75]
 K_DEPTHS = [1024, 4096, 8192]
@@ -249,7 +249,7 @@ def main(argv=None) -> int:
     t.add_argument("--out", required=True, help="where to write the table (C++ source)")
     t.add_argument("--from-report", help="rewrite the table from this saved report instead of measuring")
     t.add_argument("--exact", default="4092x4092x4092,8192x8192x8192,8192x12288x4096,8192x14336x4096,"
-                                      "8192x4096x14336",
+                                      "8192x4096x14336,32x14336x4096,64x14336x4096,128x14336x4096",
                    help="shapes (MxNxK, comma-separated) measured one by one; their entries come first")
     s = sub.add_parser("search", help="time every legal default configuration")
     s.add_argument("--workdir", required=True, help="directory for the variant libraries")

@@ -208,6 +208,17 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
 }
 
 // 128-bit streaming load that does not allocate in L1 (data used once).
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute may start while the kernel before it on the
+// stream is still running; pdl_wait() blocks until that kernel has completed
+// and its writes are visible (it returns at once without such a launch).
+// pdl_trigger() in the earlier kernel lets the dependent grid launch once every
+// CTA of the earlier grid has triggered or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float4 ldg_stream_f4(const float *p) {
     float4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"

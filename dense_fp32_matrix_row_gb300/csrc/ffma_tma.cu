@@ -39,6 +39,9 @@
 #ifndef FFMA_TAIL_SPLIT
 #define FFMA_TAIL_SPLIT 1
 #endif
+#ifndef FFMA_PDL
+#define FFMA_PDL 1   // launch the tile kernel as a programmatic dependent of the transpose
+#endif
 #ifndef FFMA_PACKED
 #define FFMA_PACKED 1
 #endif
@@ -62,6 +65,16 @@
 #endif
 #ifndef FFMA_MINB
 #define FFMA_MINB 2
+#endif
+// the 32-row configuration (index 4): k-tile depth, stages, CTAs per SM
+#ifndef FFMA_SK_BK
+#define FFMA_SK_BK 32
+#endif
+#ifndef FFMA_SK_STAGES
+#define FFMA_SK_STAGES 2
+#endif
+#ifndef FFMA_SK_MINB
+#define FFMA_SK_MINB 3
 #endif
 
 namespace sgemm_gb300 {
@@ -92,7 +105,8 @@ using Default = Cfg<FFMA_TM, FFMA_TN, FFMA_WM, FFMA_WN, FFMA_BK, FFMA_STAGES, FF
 using Wide = Cfg<8, 8, 2, 4, 32, 2, 2>;                                         // 64 x 256
 using Narrow = Cfg<8, 8, 4, 1, 32, 2, 4>;                                       // 128 x 64
 using ShallowK = Cfg<8, 8, 4, 2, 16, 4, 2>;                                     // 128 x 128, BK 16
-constexpr int kFfmaConfigs = 4;
+using Skinny = Cfg<8, 8, 1, 4, FFMA_SK_BK, FFMA_SK_STAGES, FFMA_SK_MINB>;          // 32 x 256
+constexpr int kFfmaConfigs = 5;
 
 // f(C{}) for the configuration with index `idx`.
 template <class F>
@@ -101,6 +115,7 @@ decltype(auto) with_config(int idx, F &&f) {
         case 1: return f(Wide{});
         case 2: return f(Narrow{});
         case 3: return f(ShallowK{});
+        case 4: return f(Skinny{});
         default: return f(Default{});
     }
 }
@@ -207,9 +222,9 @@ __device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int
 }
 
 // Work units.  Units 0 .. full-1 are whole tiles, tile t = unit t, in
-// row-major tile order (tiles_x tiles along N).  When the last wave of tiles
-// would leave most CTA slots idle, each of the remaining tiles is split into
-// `parts` ranges of kt_part k-tiles: unit full + r*parts + p computes part p
+// row-major tile order (tiles_x tiles along N).  When the tiles after the
+// last full wave of CTA slots would leave slots idle (see plan_units), each
+// of them is split into `parts` ranges of kt_part k-tiles: unit full + r*parts + p computes part p
 // of tile full + r, writes its partial tile to `partials`, and the unit that
 // finishes a tile last (counted in counters[r], zeroed before the launch)
 // sums the parts in part order and applies the epilogue -- no unit waits for
@@ -278,11 +293,15 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
             issued[s] = -1;
         }
         mbar_fence_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmAt);
         tma_prefetch_desc(&tmB);
+    }
+    // Launched as a programmatic dependent of the transpose: everything above
+    // overlaps its tail; A^T, and the split counters it zeroes, are read only
+    // after it has completed.
+    pdl_wait();
+    __syncthreads();
+    if (threadIdx.x == 0) {
         for (int j = 0; j < STAGES && j < nkt; ++j) issue(j);
     }
 
@@ -385,10 +404,18 @@ int ctas_per_sm() {
     return n;
 }
 
-// The work list for one call.  The tail split is used when the tiles left
-// over after the last full wave of CTA slots fill at most half a wave, each
-// part keeps at least four k-tiles, and the partial tiles fit in `capacity`
-// floats of workspace beside A^T.
+// The work list for one call.  The tiles left after the last full wave of
+// CTA slots (all tiles, when they do not fill one wave) form the tail.  The
+// tail's tiles may be split into `parts` K ranges, whichever part count
+// (1 .. 16, each part at least four k-tiles) makes the tail cheapest under
+// a simple model: the tail runs in ceil(tail*parts/slots) waves, each as
+// long as one part's k-steps plus a fixed cost per unit (the pipeline fill,
+// the partial tile's store and the last unit's sum), FFMA_SPLIT_C0 k-steps.
+// Ties keep fewer parts.  The partial tiles must fit in `capacity` floats of
+// workspace beside A^T.
+#ifndef FFMA_SPLIT_C0
+#define FFMA_SPLIT_C0 64
+#endif
 struct Plan {
     int tiles_x = 0;
     int64_t tiles = 0, full = 0;
@@ -414,17 +441,29 @@ Plan plan_units(const GemmArgs &g, int64_t at_floats, int64_t capacity) {
     const int64_t ktiles = (g.K + C::BK - 1) / C::BK;
     if (slots <= 0 || !FFMA_TAIL_SPLIT) return p;
     const int64_t rem = p.tiles % slots;
-    if (rem == 0 || 2 * rem > slots || rem > kCounterFloats) return p;
-    int parts = (int)std::min<int64_t>(std::min<int64_t>(slots / rem, kMaxParts), ktiles / 4);
+    if (rem == 0 || rem > kCounterFloats) return p;
+    // tail cost in k-steps: waves x (k-steps of a part + fixed cost)
+    auto cost = [&](int64_t parts, int64_t kt_part) {
+        return (rem * parts + slots - 1) / slots * (kt_part * C::BK + FFMA_SPLIT_C0);
+    };
+    int64_t best_cost = cost(1, ktiles);
+    Plan best = p;
     Plan q = p;
     q.full = p.tiles - rem;
-    for (; parts >= 2; --parts) {
-        q.parts = parts;
-        if (at_floats + partial_floats<C>(q) <= capacity) break;
+    const int64_t pmax = std::min<int64_t>(kMaxParts, ktiles / 4);
+    for (int64_t parts = 2; parts <= pmax; ++parts) {
+        const int64_t kt_part = (ktiles + parts - 1) / parts;
+        if ((ktiles + kt_part - 1) / kt_part != parts) continue;   // the last part would be empty
+        q.parts = (int)parts;
+        q.kt_part = (int)kt_part;
+        if (at_floats + partial_floats<C>(q) > capacity) break;  // more parts need more room
+        const int64_t c = cost(parts, kt_part);
+        if (c < best_cost) {
+            best_cost = c;
+            best = q;
+        }
     }
-    if (parts < 2) return p;
-    q.kt_part = (int)((ktiles + parts - 1) / parts);
-    return q;
+    return best;
 }
 
 template <class C>
@@ -446,10 +485,19 @@ cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt, const Pl
     ts.counters = reinterpret_cast<unsigned *>(extra);
     ts.partials = extra != nullptr ? extra + kCounterFloats : nullptr;
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
-    ffma_tma_kernel<C><<<(unsigned)p.units(), C::THREADS, C::SMEM, g.stream>>>(
-        tmAt, tmB, (int)g.M, (int)g.N, (int)g.K, g.epi(), g.C, g.ldc, c_vec4, ts, g.err,
-        g.wait_ns);
-    return cudaGetLastError();
+    // a programmatic dependent of the transpose launched just before it
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.units(), 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = g.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = FFMA_PDL;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ffma_tma_kernel<C>, tmAt, tmB, (int)g.M, (int)g.N, (int)g.K,
+                              g.epi(), g.C, g.ldc, c_vec4, ts, g.err, g.wait_ns);
 }
 
 }  // namespace

@@ -48,6 +48,9 @@ transpose_tile_kernel(int64_t R, int64_t Cc, const float *__restrict__ src, int6
                       int64_t ldd, unsigned *__restrict__ zero, int nzero) {
     constexpr bool SPLIT = OUT == kOutTf32Split;
     __shared__ float tile[TD][TD + 1];
+    // the kernel that consumes this output may be launched now; it waits
+    // for this grid to complete before it reads anything (pdl_wait)
+    pdl_trigger();
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < nzero; i += TTHREADS) zero[i] = 0u;
     const int64_t r0 = (int64_t)blockIdx.y * TD, c0 = (int64_t)blockIdx.x * TD;

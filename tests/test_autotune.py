@@ -15,7 +15,7 @@ TABLE = os.path.join(ROOT, "dense_fp32_matrix_row_gb300", "csrc", "ffma_tuning.i
 
 # (TM, TN, WM, WN, BK, STAGES, MINB) of the configurations compiled into the library
 COMPILED = [(8, 8, 4, 2, 32, 2, 2), (8, 8, 2, 4, 32, 2, 2), (8, 8, 4, 1, 32, 2, 4),
-            (8, 8, 4, 2, 16, 4, 2)]
+            (8, 8, 4, 2, 16, 4, 2), (8, 8, 1, 4, 32, 2, 3)]
 
 
 @pytest.fixture(scope="module")

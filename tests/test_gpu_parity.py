@@ -326,11 +326,11 @@ def test_pair_tiles(mode, M, N, K):
 # ---------------------------------------------------------------- FFMA tile configurations
 # Every configuration compiled into the library (the autotuner's choices),
 # forced, on shapes with ragged edges, a split last wave and beta != 0.
-@pytest.mark.parametrize("cfg", range(4))
+@pytest.mark.parametrize("cfg", range(5))
 @pytest.mark.parametrize("M,N,K", [(300, 260, 516), (1500, 1100, 700), (129, 1000, 77),
-                                   (2300, 2352, 1001)])
+                                   (2300, 2352, 1001), (31, 3000, 2050)])
 def test_every_ffma_config(cfg, M, N, K):
-    assert len(sg.ffma_configs()) == 4
+    assert len(sg.ffma_configs()) == 5
     A, B, C0 = make_inputs(M, N, K, "normal", seed=M + cfg, beta=0.5)
     ldb = (N + 3) // 4 * 4
     prev = sg.ffma_force_config(cfg)
@@ -574,6 +574,29 @@ def test_split_last_wave(M, N, K, beta, ldc_pad):
         assert sg.status() == sg.OK
         outs.append(dC.cpu().numpy())
     assert np.array_equal(outs[0], outs[1])
+
+
+# Skinny products, 17 <= M <= 128 (the band between the decode kernel and
+# full tiles: 32-row tiles, split along K so the few tiles fill the GPU);
+# ragged M, N and K, every output compared.
+SK_M = [17, 24, 31, 32, 33, 48, 63, 64, 65, 100, 127, 128]
+SK_NK = [(257, 100), (3001, 1031), (14336, 4096)]
+
+
+@pytest.mark.parametrize("N,K", SK_NK)
+@pytest.mark.parametrize("M", SK_M)
+def test_skinny_band(M, N, K):
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=31 * M + N + K, beta=0.5, sigma_b=0.02)
+    ldb = (N + 3) // 4 * 4
+    _, chosen = run_checked(sg, A, B, C0, 1.0, 0.5, lds=(K, ldb, N))
+    assert chosen == TMA
+
+
+@pytest.mark.parametrize("M", [17, 32, 64, 128])
+def test_skinny_band_integers_exact(M):
+    A, B, C0 = make_inputs(M, 14336, 4096, "int", seed=M, beta=-1.0)
+    _, chosen = run_checked(sg, A, B, C0, 1.0, -1.0, exact=True)
+    assert chosen == TMA
 
 
 def test_large_small_integers_exact():
