@@ -207,7 +207,6 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 128-bit streaming load that does not allocate in L1 (data used once).
 // Programmatic dependent launch.  A kernel launched with the programmatic
 // stream-serialization attribute may start while the kernel before it on the
 // stream is still running; pdl_wait() blocks until that kernel has completed
@@ -219,6 +218,7 @@ __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// 128-bit streaming load that does not allocate in L1 (data used once).
 __device__ __forceinline__ float4 ldg_stream_f4(const float *p) {
     float4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"

@@ -222,28 +222,44 @@ __device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int
 }
 
 // Work units.  Units 0 .. full-1 are whole tiles, tile t = unit t, in
-// row-major tile order (tiles_x tiles along N).  When the tiles after the
-// last full wave of CTA slots would leave slots idle (see plan_units), each
-// of them is split into `parts` ranges of kt_part k-tiles: unit full + r*parts + p computes part p
-// of tile full + r, writes its partial tile to `partials`, and the unit that
-// finishes a tile last (counted in counters[r], zeroed before the launch)
-// sums the parts in part order and applies the epilogue -- no unit waits for
-// another.
-struct TailSplit {
+// row-major tile order (tiles_x tiles along N).  The tiles after the last
+// full wave of CTA slots -- all tiles, when they do not fill one wave -- form
+// the tail.  When plan_units finds it cheaper, the tail is divided by work
+// rather than by tile: its rem x ktiles k-tile iterations, taken tile by tile
+// in k order, are dealt out in contiguous runs of `span` iterations to units
+// full, full + 1, ..., so every tail unit gets the same amount of work
+// whatever the tile count (the "stream-K" division).  A unit's run may end
+// part of one tile and start the next.  For each tile it touches without
+// covering it whole, the unit writes its partial tile to a slot of
+// `partials` and counts the tile's arrival in counters[tile - full] (zeroed
+// before the launch); the unit that completes the count sums the tile's
+// partial tiles in unit order and runs the epilogue.  No unit waits for
+// another, and the sum order does not depend on timing.
+struct TailPlan {
     int tiles_x;
-    int full;
-    int parts;
-    int kt_part;
-    float *partials;      // [(tiles - full) * parts][THREADS * TM * TN]
-    unsigned *counters;   // [tiles - full]
+    int full;             // whole-tile units
+    int span;             // k-tile iterations per tail unit; 0: no tail division
+    int tail_iters;       // rem * ktiles
+    float *partials;      // two slots per tail unit, each [TM * TN / 4][THREADS] float4
+    unsigned *counters;   // [rem]
 };
+
+// Slot of tail unit v's partial tile of tail tile t: 2v + 1 when v's run ends
+// in t (inside it or at its end), 2v when v's run goes on past t.  A run is
+// shorter than a tile, so it touches at most two tiles and they get
+// different slots.
+__device__ __forceinline__ int partial_slot(int v, int t, int span, int ktiles, int iters) {
+    const int end = min((v + 1) * span, iters);
+    return 2 * v + (end <= (t + 1) * ktiles ? 1 : 0);
+}
 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, C::MINB)
 ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant__ CUtensorMap tmB,
                 int M, int N, int K, Epilogue ep, float *__restrict__ Cm, int64_t ldc,
-                int c_vec4, TailSplit ts, unsigned *err, uint64_t wait_ns) {
+                int c_vec4, TailPlan tp, unsigned *err, uint64_t wait_ns) {
     constexpr int TM = C::TM, TN = C::TN, BK = C::BK, BM = C::BM, BN = C::BN, STAGES = C::STAGES;
+    constexpr int NV = TM * TN / 4;   // float4s of a lane's partial tile
     extern __shared__ unsigned char smem_raw[];
     __shared__ unsigned s_prev;
     const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127);
@@ -255,26 +271,27 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ktiles = (K + BK - 1) / BK;
-    const int unit = blockIdx.x;
-    int tile = unit, part = -1, kt0 = 0, kt1 = ktiles;
-    if (unit >= ts.full) {
-        const int v = unit - ts.full;
-        tile = ts.full + v / ts.parts;
-        part = v % ts.parts;
-        kt0 = part * ts.kt_part;
-        kt1 = min(kt0 + ts.kt_part, ktiles);
-    }
-    const int m0 = (tile / ts.tiles_x) * BM, n0 = (tile % ts.tiles_x) * BN;
-    const int nkt = kt1 > kt0 ? kt1 - kt0 : 0;
-
-    // Copy local k-tile j (k-tile kt0 + j) into stage j % STAGES (one thread).
+    // This unit's k-tile iterations j = 0 .. n-1: k-tile j of tile blockIdx.x,
+    // or, for a tail unit v = blockIdx.x - full, iteration v*span + j of the
+    // tail (tile full + i/ktiles, k-tile i%ktiles for i = v*span + j).
+    const bool in_tail = (int)blockIdx.x >= tp.full;
+    const int n = in_tail ? min(tp.span, tp.tail_iters - ((int)blockIdx.x - tp.full) * tp.span) : ktiles;
+    // Where the copies of local k-tile j go, kept in shared memory rather than
+    // in every thread's registers (only the issuing thread reads them): tile
+    // origin (m0, n0) and first k-tile of the unit's first tile, the j at
+    // which its second tile starts (n if none), and that tile's origin.
+    __shared__ int s_iss[6];
     auto issue = [&](int j) {
         const int s = j % STAGES;
         issued[s] = j;
+        const volatile int *q = s_iss;
+        const bool second = j >= q[3];
+        const int m0 = second ? q[4] : q[0], n0 = second ? q[5] : q[1];
+        const int kt = second ? j - q[3] : q[2] + j;
         const uint32_t fb = smem_u32(&full[s]);
         mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-        tma_load_2d(smem_u32(sA + s * C::A_STAGE), &tmAt, fb, m0, (kt0 + j) * BK);
-        tma_load_2d(smem_u32(sB + s * C::B_STAGE), &tmB, fb, n0, (kt0 + j) * BK);
+        tma_load_2d(smem_u32(sA + s * C::A_STAGE), &tmAt, fb, m0, kt * BK);
+        tma_load_2d(smem_u32(sB + s * C::B_STAGE), &tmB, fb, n0, kt * BK);
     };
     // After a failed wait: wait for every copy issued so far, so that none
     // lands in this block's shared memory after the block has exited.
@@ -292,17 +309,31 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
             arrived[s] = 0;
             issued[s] = -1;
         }
+        int t0 = blockIdx.x, kt0 = 0, jsw = n, t1 = 0;
+        if (in_tail) {
+            const int i0 = ((int)blockIdx.x - tp.full) * tp.span;
+            t0 = tp.full + i0 / ktiles;
+            kt0 = i0 % ktiles;
+            jsw = min(n, ktiles - kt0);
+            t1 = t0 + 1;
+        }
+        s_iss[0] = (t0 / tp.tiles_x) * BM;
+        s_iss[1] = (t0 % tp.tiles_x) * BN;
+        s_iss[2] = kt0;
+        s_iss[3] = jsw;
+        s_iss[4] = (t1 / tp.tiles_x) * BM;
+        s_iss[5] = (t1 % tp.tiles_x) * BN;
         mbar_fence_init();
         tma_prefetch_desc(&tmAt);
         tma_prefetch_desc(&tmB);
     }
     // Launched as a programmatic dependent of the transpose: everything above
-    // overlaps its tail; A^T, and the split counters it zeroes, are read only
+    // overlaps its tail; A^T, and the tail counters it zeroes, are read only
     // after it has completed.
     pdl_wait();
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int j = 0; j < STAGES && j < nkt; ++j) issue(j);
+        for (int j = 0; j < STAGES && j < n; ++j) issue(j);
     }
 
     const int wm = warp / C::WN, wn = warp % C::WN;
@@ -314,75 +345,96 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+        for (int jj = 0; jj < TN; ++jj) acc[i][jj] = 0.0f;
 
-    bool failed = false;
-    for (int j = 0; j < nkt; ++j) {
-        const int s = j % STAGES;
-        if (!mbar_wait(smem_u32(&full[s]), (j / STAGES) & 1, wait_ns)) {
-            failed = true;
-            if (lane == 0) record_error(err, kErrWaitTimeout);
-            break;
-        }
-        compute_stage<C>(acc, sA + s * C::A_STAGE + arow, sB + s * C::B_STAGE + bcol);
-        // Release the stage; the last warp to do so refills it STAGES k-tiles ahead.
-        __syncwarp();
-        if (lane == 0) {
-            __threadfence_block();
-            if (atomicAdd(&arrived[s], 1u) == C::WARPS - 1) {
-                arrived[s] = 0;
-                if (j + STAGES < nkt) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue(j + STAGES);
+    // Segments: the k-tiles a unit computes for one tile (a whole-tile unit
+    // has one; a tail unit one or two).  The k loop of a segment is the
+    // kernel's hot loop; segment ends are block-wide (a failed wait in any
+    // warp is seen there and skips every later store).
+    bool any_failed = false;
+    for (int j0 = 0; j0 < n;) {
+        const int j1 = j0 == 0 ? s_iss[3] : n;   // the first tile's k-tiles, then the rest
+        bool failed = false;
+        for (int j = j0; j < j1; ++j) {
+            const int s = j % STAGES;
+            if (!mbar_wait(smem_u32(&full[s]), (j / STAGES) & 1, wait_ns)) {
+                failed = true;
+                if (lane == 0) record_error(err, kErrWaitTimeout);
+                break;
+            }
+            compute_stage<C>(acc, sA + s * C::A_STAGE + arow, sB + s * C::B_STAGE + bcol);
+            // Release the stage; the last warp to do so refills it STAGES k-tiles ahead.
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                if (atomicAdd(&arrived[s], 1u) == C::WARPS - 1) {
+                    arrived[s] = 0;
+                    if (j + STAGES < n) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue(j + STAGES);
+                    }
                 }
             }
         }
+        any_failed = __syncthreads_or(failed) != 0;
+        if (any_failed) break;
+
+        const int m0 = s_iss[j0 == 0 ? 0 : 4], n0 = s_iss[j0 == 0 ? 1 : 5];
+        if (j1 - j0 == ktiles) {
+            store_tile<C>(acc, m0, n0, arow, bcol, M, N, ep, Cm, ldc, c_vec4);
+        } else {
+            // partial tile, thread-interleaved so that each warp writes whole lines
+            const int v = (int)blockIdx.x - tp.full;
+            const int t = (v * tp.span + j0) / ktiles;   // tail tile of this segment
+            float4 *mine = reinterpret_cast<float4 *>(tp.partials) +
+                           (size_t)partial_slot(v, t, tp.span, ktiles, tp.tail_iters) * NV * C::THREADS;
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int h = 0; h < TN / 4; ++h)
+                    __stcg(mine + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x,
+                           make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
+                                       acc[i][4 * h + 3]));
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) s_prev = atomicAdd(&tp.counters[t], 1u);
+            __syncthreads();
+            const int v0 = t * ktiles / tp.span, v1 = ((t + 1) * ktiles - 1) / tp.span;
+            if (s_prev == (unsigned)(v1 - v0)) {
+                // last one in: sum the partial tiles of units v0 .. v1 in that
+                // order (this unit's included), whichever unit arrived last
+                __threadfence();
+                for (int w = v0; w <= v1; ++w) {
+                    const float4 *src = reinterpret_cast<const float4 *>(tp.partials) +
+                                        (size_t)partial_slot(w, t, tp.span, ktiles, tp.tail_iters) * NV *
+                                            C::THREADS;
+#pragma unroll
+                    for (int i = 0; i < TM; ++i)
+#pragma unroll
+                        for (int h = 0; h < TN / 4; ++h) {
+                            const float4 q = __ldcg(src + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x);
+                            if (w == v0) {
+                                acc[i][4 * h] = q.x; acc[i][4 * h + 1] = q.y;
+                                acc[i][4 * h + 2] = q.z; acc[i][4 * h + 3] = q.w;
+                            } else {
+                                acc[i][4 * h] += q.x; acc[i][4 * h + 1] += q.y;
+                                acc[i][4 * h + 2] += q.z; acc[i][4 * h + 3] += q.w;
+                            }
+                        }
+                }
+                store_tile<C>(acc, m0, n0, arow, bcol, M, N, ep, Cm, ldc, c_vec4);
+            }
+        }
+        j0 = j1;
+        if (j0 < n) {
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int jj = 0; jj < TN; ++jj) acc[i][jj] = 0.0f;
+        }
     }
-    // Every warp is past the loop, so `issued` no longer changes.
-    const bool any_failed = __syncthreads_or(failed) != 0;
+    // Every warp is past its k loop, so `issued` no longer changes.
     if (any_failed && threadIdx.x == 0) drain();
-
-    // ---------------------------------------------------------------- epilogue
-    if (part < 0) {
-        if (!any_failed) store_tile<C>(acc, m0, n0, arow, bcol, M, N, ep, Cm, ldc, c_vec4);
-        return;
-    }
-    // Partial tile, thread-interleaved so that each warp writes whole lines.
-    constexpr int NV = TM * TN / 4;
-    float4 *mine = reinterpret_cast<float4 *>(ts.partials) + (size_t)(unit - ts.full) * NV * C::THREADS;
-#pragma unroll
-    for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int h = 0; h < TN / 4; ++h)
-            __stcg(mine + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x,
-                   make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]));
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) s_prev = atomicAdd(&ts.counters[tile - ts.full], 1u);
-    __syncthreads();
-    if (s_prev != (unsigned)(ts.parts - 1)) return;
-    __threadfence();
-    // Last part in: sum parts 0 .. parts-1 in that order (own part included),
-    // independent of which unit arrived last.
-    const float4 *first = reinterpret_cast<const float4 *>(ts.partials) +
-                          (size_t)(tile - ts.full) * ts.parts * NV * C::THREADS;
-    for (int q = 0; q < ts.parts; ++q) {
-        const float4 *src = first + (size_t)q * NV * C::THREADS;
-#pragma unroll
-        for (int i = 0; i < TM; ++i)
-#pragma unroll
-            for (int h = 0; h < TN / 4; ++h) {
-                const float4 v = __ldcg(src + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x);
-                if (q == 0) {
-                    acc[i][4 * h] = v.x; acc[i][4 * h + 1] = v.y;
-                    acc[i][4 * h + 2] = v.z; acc[i][4 * h + 3] = v.w;
-                } else {
-                    acc[i][4 * h] += v.x; acc[i][4 * h + 1] += v.y;
-                    acc[i][4 * h + 2] += v.z; acc[i][4 * h + 3] += v.w;
-                }
-            }
-    }
-    store_tile<C>(acc, m0, n0, arow, bcol, M, N, ep, Cm, ldc, c_vec4);
 }
 
 // CTAs of the kernel one SM holds, per device (0 until asked).
@@ -404,31 +456,33 @@ int ctas_per_sm() {
     return n;
 }
 
-// The work list for one call.  The tiles left after the last full wave of
-// CTA slots (all tiles, when they do not fill one wave) form the tail.  The
-// tail's tiles may be split into `parts` K ranges, whichever part count
-// (1 .. 16, each part at least four k-tiles) makes the tail cheapest under
-// a simple model: the tail runs in ceil(tail*parts/slots) waves, each as
-// long as one part's k-steps plus a fixed cost per unit (the pipeline fill,
-// the partial tile's store and the last unit's sum), FFMA_SPLIT_C0 k-steps.
-// Ties keep fewer parts.  The partial tiles must fit in `capacity` floats of
-// workspace beside A^T.
+// The work list for one call (see TailPlan).  The tail -- the tiles left
+// after the last full wave of CTA slots, all tiles when they do not fill one
+// wave -- is divided by work when that is cheaper under a simple model: run
+// as whole tiles, it takes one wave of ktiles k-tiles plus a fixed cost per
+// unit (pipeline fill, epilogue); divided, one wave of `span` k-tiles plus two
+// fixed costs (a unit may end one tile and start the next), where span is
+// the tail's iterations over the CTA slots, at least four k-tiles and fewer
+// than ktiles.  The fixed cost is FFMA_SPLIT_C0 k-steps.  The partial tiles
+// (two slots per tail unit) must fit in `capacity` floats of workspace beside
+// A^T; a longer span (fewer units) is taken when they do not.
 #ifndef FFMA_SPLIT_C0
 #define FFMA_SPLIT_C0 64
 #endif
 struct Plan {
     int tiles_x = 0;
     int64_t tiles = 0, full = 0;
-    int parts = 1, kt_part = 0;
-    int64_t tail() const { return tiles - full; }
-    int64_t units() const { return full + tail() * parts; }
+    int span = 0;              // 0: whole tiles only
+    int64_t tail_units = 0;
+    int64_t rem() const { return tiles - full; }
+    int64_t units() const { return full + tail_units; }
 };
 constexpr int64_t kCounterFloats = 1024;   // counters reserved after A^T
-constexpr int64_t kMaxParts = 16;
+constexpr int64_t kMinSpan = 4;            // k-tiles per tail unit, at least
 
 template <class C>
 int64_t partial_floats(const Plan &p) {
-    return p.parts > 1 ? kCounterFloats + p.tail() * p.parts * (int64_t)C::BM * C::BN : 0;
+    return p.span > 0 ? kCounterFloats + 2 * p.tail_units * (int64_t)C::BM * C::BN : 0;
 }
 
 template <class C>
@@ -442,28 +496,17 @@ Plan plan_units(const GemmArgs &g, int64_t at_floats, int64_t capacity) {
     if (slots <= 0 || !FFMA_TAIL_SPLIT) return p;
     const int64_t rem = p.tiles % slots;
     if (rem == 0 || rem > kCounterFloats) return p;
-    // tail cost in k-steps: waves x (k-steps of a part + fixed cost)
-    auto cost = [&](int64_t parts, int64_t kt_part) {
-        return (rem * parts + slots - 1) / slots * (kt_part * C::BK + FFMA_SPLIT_C0);
-    };
-    int64_t best_cost = cost(1, ktiles);
-    Plan best = p;
+    const int64_t iters = rem * ktiles;
+    const int64_t whole_cost = ktiles * C::BK + FFMA_SPLIT_C0;
     Plan q = p;
     q.full = p.tiles - rem;
-    const int64_t pmax = std::min<int64_t>(kMaxParts, ktiles / 4);
-    for (int64_t parts = 2; parts <= pmax; ++parts) {
-        const int64_t kt_part = (ktiles + parts - 1) / parts;
-        if ((ktiles + kt_part - 1) / kt_part != parts) continue;   // the last part would be empty
-        q.parts = (int)parts;
-        q.kt_part = (int)kt_part;
-        if (at_floats + partial_floats<C>(q) > capacity) break;  // more parts need more room
-        const int64_t c = cost(parts, kt_part);
-        if (c < best_cost) {
-            best_cost = c;
-            best = q;
-        }
+    for (int64_t span = std::max(kMinSpan, (iters + slots - 1) / slots); span < ktiles; ++span) {
+        if (span * C::BK + 2 * FFMA_SPLIT_C0 >= whole_cost) break;   // no cheaper than whole tiles
+        q.span = (int)span;
+        q.tail_units = (iters + span - 1) / span;
+        if (at_floats + partial_floats<C>(q) <= capacity) return q;   // the shortest span that fits
     }
-    return best;
+    return p;
 }
 
 template <class C>
@@ -477,13 +520,13 @@ cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt, const Pl
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     if (p.units() > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    TailSplit ts;
-    ts.tiles_x = p.tiles_x;
-    ts.full = (int)p.full;
-    ts.parts = p.parts;
-    ts.kt_part = p.kt_part;
-    ts.counters = reinterpret_cast<unsigned *>(extra);
-    ts.partials = extra != nullptr ? extra + kCounterFloats : nullptr;
+    TailPlan tp;
+    tp.tiles_x = p.tiles_x;
+    tp.full = (int)p.full;
+    tp.span = p.span;
+    tp.tail_iters = (int)(p.rem() * ((g.K + C::BK - 1) / C::BK));
+    tp.counters = reinterpret_cast<unsigned *>(extra);
+    tp.partials = extra != nullptr ? extra + kCounterFloats : nullptr;
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
     // a programmatic dependent of the transpose launched just before it
     cudaLaunchConfig_t cfg = {};
@@ -497,7 +540,7 @@ cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt, const Pl
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, ffma_tma_kernel<C>, tmAt, tmB, (int)g.M, (int)g.N, (int)g.K,
-                              g.epi(), g.C, g.ldc, c_vec4, ts, g.err, g.wait_ns);
+                              g.epi(), g.C, g.ldc, c_vec4, tp, g.err, g.wait_ns);
 }
 
 }  // namespace
@@ -547,10 +590,10 @@ cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace, int64_t capacit
     return with_config(ffma_config_for(g.M, g.N), [&](auto c) -> cudaError_t {
         using C = decltype(c);
         const Plan p = plan_units<C>(g, at, capacity);
-        float *extra = p.parts > 1 ? workspace + at : nullptr;
+        float *extra = p.span > 0 ? workspace + at : nullptr;
         cudaError_t e = launch_transpose(g.M, g.K, g.A, g.lda, workspace, ldt, g.stream,
                                          reinterpret_cast<unsigned *>(extra),
-                                         (int)(p.parts > 1 ? p.tail() : 0));
+                                         (int)(p.span > 0 ? p.rem() : 0));
         if (e != cudaSuccess) return e;
         return launch_cfg<C>(g, workspace, ldt, p, extra);
     });
