@@ -160,6 +160,14 @@ WORKLOADS = {
                       a=("normal", 0.0, 1.0), b=("normal", 0.0, 0.02), c=None),
     "decode_m16": dict(M=16, N=14336, K=4096, alpha=1.0, beta=0.0, seed=3,
                        a=("normal", 0.0, 1.0), b=("normal", 0.0, 0.02), c=None),
+    # skinny products on the decode shapes' N, K and B (the band between
+    # the decode kernel and full tiles)
+    "skinny_m32": dict(M=32, N=14336, K=4096, alpha=1.0, beta=0.0, seed=3,
+                       a=("normal", 0.0, 1.0), b=("normal", 0.0, 0.02), c=None),
+    "skinny_m64": dict(M=64, N=14336, K=4096, alpha=1.0, beta=0.0, seed=3,
+                       a=("normal", 0.0, 1.0), b=("normal", 0.0, 0.02), c=None),
+    "skinny_m128": dict(M=128, N=14336, K=4096, alpha=1.0, beta=0.0, seed=3,
+                        a=("normal", 0.0, 1.0), b=("normal", 0.0, 0.02), c=None),
     "prefill_qkv": dict(M=8192, N=12288, K=4096, alpha=1.0, beta=0.0, seed=4,
                         a=("normal", 0.0, 1.0), b=("normal", 0.0, 0.02), c=None),
     "prefill_up": dict(M=8192, N=14336, K=4096, alpha=1.0, beta=0.0, seed=4,
