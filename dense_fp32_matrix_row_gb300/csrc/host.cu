@@ -13,6 +13,7 @@
 // ordered like any other work on that stream.
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -100,9 +101,14 @@ int b_parts(int64_t M, int64_t rows, int64_t K, bool uses_ab) {
     return 1;
 }
 
-// Rows per panel.  Panels must stay large enough to fill the GPU on their
-// own: the FFMA kernel's tiles are 128 rows tall and a panel of ~1000 rows
-// at N ~ 4000 is about one wave.  Skinny products run as one panel.
+// Rows per panel.  Each panel adds a fixed cost (its own kernel ramp, tail
+// and transposition of A; measured on GB300 about 10 us per 1024 of K), and
+// the first panel's copy up and the last panel's copy down are not hidden
+// behind any compute.  With t_row the copy time of one row (A and C up at
+// about 209 GB/s, C down at about 192 GB/s) the count that balances the two,
+// M * t_row / P against P * t_panel, is sqrt(M * t_row / t_panel), at most 8.
+// Measured at 4092^3 (ms per call by panel count): 2: 2.94, 3: 2.90,
+// 4: 2.84, 5: 2.77, 6: 2.79, 8: 2.78.  Skinny products run as one panel.
 int64_t panel_rows(int64_t M, int64_t N, int64_t K, bool uses_ab) {
     const int forced = g_panels.load();
     int64_t P;
@@ -111,11 +117,9 @@ int64_t panel_rows(int64_t M, int64_t N, int64_t K, bool uses_ab) {
     } else if (!uses_ab || M <= 256) {
         P = 1;
     } else {
-        // about 2^22 output elements (four waves of 128 x 64 tiles at least)
-        // per panel, at most 8 panels
-        const int64_t per = std::max<int64_t>(1, (int64_t(1) << 22) / std::max<int64_t>(N, 1));
-        P = std::min<int64_t>(8, std::max<int64_t>(1, M / std::max<int64_t>(per, 128)));
-        (void)K;
+        const double t_row_us = (double)(K + N) * 4.0 / 209e3 + (double)N * 4.0 / 192e3;
+        const double t_panel_us = 10.0 * (double)K / 1024.0;
+        P = std::min<int64_t>(8, std::max<int64_t>(1, std::llround(std::sqrt((double)M * t_row_us / t_panel_us))));
     }
     P = std::max<int64_t>(1, std::min<int64_t>(P, M));
     int64_t rows = (M + P - 1) / P;

@@ -295,8 +295,9 @@ int sgemm_selftest_wait(int64_t ns, void *stream);
  * Memory: the library keeps one device buffer per (device, stream) holding
  * B and two panels of A and C (grown with cudaMallocAsync on `stream`; freed
  * by sgemm_release_workspaces), plus two copy streams and a few events.
- * Panel rows: a multiple of 128 chosen so each panel still fills the GPU
- * (sgemm_host_panel_rows reports it; sgemm_host_set_panels overrides the
+ * Panel rows: a multiple of 128; the count (at most 8) balances the copies
+ * that no compute hides (the first panel's up, the last panel's down) against
+ * a fixed cost per panel (sgemm_host_panel_rows reports it; sgemm_host_set_panels overrides the
  * panel count, 0 restores the library's choice and the previous setting is
  * returned).  Products with M <= 256 or without an A@B term run as one panel.
  * Errors: those of sgemm(); SGEMM_ERR_CAPTURE while `stream` is being
