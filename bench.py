@@ -33,6 +33,7 @@ import datetime as _dt
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import tempfile
@@ -66,12 +67,23 @@ KERNEL_SOURCES = {
 }
 
 
+_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def _code_only(text: str) -> str:
+    """C++ source without its comments and with whitespace collapsed, so that
+    editing a comment does not count as changing a kernel."""
+    text = _TOKENS.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return " ".join(text.split())
+
+
 def source_hash(kernel: str) -> str:
+    """Hash of the code (comments excluded) of the files a kernel is built from."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
         p = os.path.join(ROOT, rel)
         if os.path.exists(p):
-            h.update(open(p, "rb").read())
+            h.update(_code_only(open(p, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

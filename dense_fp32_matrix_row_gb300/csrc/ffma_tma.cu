@@ -27,7 +27,14 @@
 //    拆解（一）", section "共享内存的内部结构：32 个 bank");
 //  * K tails and M/N edge tiles are zero-filled by TMA (out-of-range box
 //    elements read as 0) and the epilogue guards its stores; the epilogue
-//    applies C = act(alpha*acc + beta*C + bias), reading C only when beta != 0.
+//    applies C = act(alpha*acc + beta*C + bias), reading C only when beta != 0;
+//  * the grid is a 1-D list of work units: whole tiles for the full waves of
+//    CTA slots, then the tail divided by work -- equal runs of k-tile
+//    iterations, summed through partial tiles in a fixed order (the split-K
+//    of "CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section "10", see
+//    TailPlan and plan_units);
+//  * the kernel is launched as a programmatic dependent of the transpose that
+//    writes its A^T, so its set-up overlaps the transpose's tail.
 //
 // Lane (ty, tx) of warp (wm, wn) owns rows    wm*4*TM + 16*(i/4) + 4*ty + i%4   (i < TM)
 //                                 and columns wn*8*TN + 32*(j/4) + 4*tx + j%4   (j < TN).
