@@ -62,7 +62,7 @@ def test_argument_errors(L):
     # C overlapping A or B (address ranges in bytes)
     assert sel(64, 64, 64, A=1 << 20, C=(1 << 20) + 4 * 100) == sg.ERR_ALIAS
     assert sel(64, 64, 64, B=1 << 20, C=(1 << 20) - 4 * 100) == sg.ERR_ALIAS
-    assert sel(64, 64, 64, A=1 << 20, B=1 << 22, C=1 << 24) == sg.KERNEL_FFMA_TMA
+    assert sel(64, 64, 64, A=1 << 20, B=1 << 22, C=1 << 24) == sg.KERNEL_FFMA_GENERIC
     # enormous sizes are rejected instead of overflowing offsets
     assert sel(1 << 40, 1 << 20, 4, A=1 << 20, B=1 << 22, C=1 << 24) == sg.ERR_BAD_DIM
 
@@ -79,16 +79,20 @@ def test_kernel_choice(L):
     a, b, c = 1 << 20, 1 << 26, 1 << 30
     for M in (1, 4, 16):
         assert sel(M, 14336, 4096, A=a, B=b, C=c) == sg.KERNEL_DECODE
-    assert sel(17, 64, 64, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA
+    assert sel(17, 640, 640, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA
     assert sel(4092, 4092, 4092, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA
+    # tiny products (at most 2^21 multiply-adds) take the one-launch plain-load kernel
+    assert sel(128, 128, 128, A=a, B=b, C=c) == sg.KERNEL_FFMA_GENERIC
+    assert sel(17, 64, 64, A=a, B=b, C=c) == sg.KERNEL_FFMA_GENERIC
+    assert sel(129, 128, 128, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA
     # B misaligned or ldb % 4 != 0 -> plain-load kernel; A may be anything
     # (the TMA path reads A through its transposed copy)
-    assert sel(128, 128, 128, A=a + 4, B=b, C=c) == sg.KERNEL_FFMA_TMA
-    assert sel(128, 128, 127, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA       # lda = 127
-    assert sel(128, 128, 128, A=a, B=b + 8, C=c) == sg.KERNEL_FFMA_GENERIC
-    assert sel(128, 130, 128, A=a, B=b, C=c) == sg.KERNEL_FFMA_GENERIC   # ldb = 130
+    assert sel(256, 128, 128, A=a + 4, B=b, C=c) == sg.KERNEL_FFMA_TMA
+    assert sel(256, 128, 127, A=a, B=b, C=c) == sg.KERNEL_FFMA_TMA       # lda = 127
+    assert sel(256, 128, 128, A=a, B=b + 8, C=c) == sg.KERNEL_FFMA_GENERIC
+    assert sel(256, 130, 128, A=a, B=b, C=c) == sg.KERNEL_FFMA_GENERIC   # ldb = 130
     # C alignment does not matter for the choice (the epilogue adapts)
-    assert sel(128, 128, 128, A=a, B=b, C=c + 4) == sg.KERNEL_FFMA_TMA
+    assert sel(256, 128, 128, A=a, B=b, C=c + 4) == sg.KERNEL_FFMA_TMA
 
 
 def test_tensor_core_modes(L):

@@ -149,17 +149,18 @@ def test_nan_in_inputs_propagates():
 
 # ---------------------------------------------------------------- layouts
 @pytest.mark.parametrize("lds,offsets,expect", [
-    ((70, 53, 61), (0, 0, 0), GEN),        # ld % 4 != 0 everywhere
-    ((68, 52, 61), (0, 0, 0), TMA),        # A, B TMA-able, C scalar epilogue
-    ((68, 52, 56), (0, 0, 1), TMA),        # C misaligned by one float
-    ((68, 52, 56), (1, 0, 0), TMA),        # A misaligned: read through its transposed copy
-    ((70, 52, 56), (0, 0, 0), TMA),        # lda % 4 != 0: likewise
-    ((68, 52, 56), (0, 2, 0), GEN),        # B misaligned
-    ((68, 53, 56), (0, 0, 0), GEN),        # ldb % 4 != 0
-    ((64, 48, 48), (0, 0, 0), TMA),        # dense
+    ((170, 53, 61), (0, 0, 0), GEN),       # ld % 4 != 0 everywhere
+    ((168, 52, 61), (0, 0, 0), TMA),       # A, B TMA-able, C scalar epilogue
+    ((168, 52, 56), (0, 0, 1), TMA),       # C misaligned by one float
+    ((168, 52, 56), (1, 0, 0), TMA),       # A misaligned: read through its transposed copy
+    ((170, 52, 56), (0, 0, 0), TMA),       # lda % 4 != 0: likewise
+    ((168, 52, 56), (0, 2, 0), GEN),       # B misaligned
+    ((168, 53, 56), (0, 0, 0), GEN),       # ldb % 4 != 0
+    ((164, 48, 48), (0, 0, 0), TMA),       # dense
 ])
 def test_leading_dims_and_alignment(lds, offsets, expect):
-    M, N, K = 150, 48, 64
+    # more than 2^21 multiply-adds, so the choice is not the tiny-product one
+    M, N, K = 300, 48, 164
     A, B, C0 = make_inputs(M, N, K, "normal", seed=13, beta=0.5)
     _, chosen = run_checked(sg, A, B, C0, 1.0, 0.5, lds=lds, offsets=offsets)
     assert chosen == expect
@@ -589,7 +590,8 @@ def test_skinny_band(M, N, K):
     A, B, C0 = make_inputs(M, N, K, "normal", seed=31 * M + N + K, beta=0.5, sigma_b=0.02)
     ldb = (N + 3) // 4 * 4
     _, chosen = run_checked(sg, A, B, C0, 1.0, 0.5, lds=(K, ldb, N))
-    assert chosen == TMA
+    # products of at most 2^21 multiply-adds take the one-launch plain-load kernel
+    assert chosen == (GEN if M * N * K <= 1 << 21 else TMA)
 
 
 @pytest.mark.parametrize("M", [17, 32, 64, 128])
