@@ -363,11 +363,11 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
         return e0.elapsed_time(e1) / n
 
     def graph_ms(fns):
-        """Mean ms per call of the calls `fns` captured in one CUDA graph
-        (after one warm replay)."""
+        """Mean ms per call of the calls `fns` captured in one CUDA graph:
+        the median of three replays after one warm replay."""
         graph = capture(fns)
         replay_ms(graph, len(fns))
-        ms = replay_ms(graph, len(fns))
+        ms = float(np.median([replay_ms(graph, len(fns)) for _ in range(3)]))
         del graph
         return ms
 
