@@ -107,12 +107,14 @@ extern "C" {
  *
  * Shapes with M <= 16 run the split-K streaming kernel (the decode regime of
  * "GPU GEMM 优化完全拆解（一）", section "LLM 推理本质上是 GEMM 的串联"); the rest
- * run the tiled FFMA kernel.  When the tiles left after the last full wave of
- * resident blocks fill at most half a wave, each of those tiles is split into
- * 2-16 ranges of K whose partial tiles are summed in range order (the
- * split-K reduction of "CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section
- * "10", applied to the last wave only).  The result is deterministic: the
- * same inputs give the same bits on every call on the same GPU model.
+ * run the tiled FFMA kernel (products of at most 2^21 multiply-adds, such as
+ * 128^3, the plain-load tiled kernel in a single launch).  The tiles left
+ * after the last full wave of resident blocks -- all tiles, when they do not
+ * fill one wave -- may be divided by work: equal runs of K iterations whose
+ * partial tiles are summed in a fixed order (the split-K reduction of "CUDA
+ * 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section "10", applied to the tail
+ * only).  The result is deterministic: the same inputs give the same bits on
+ * every call on the same GPU model.
  * CUDA graphs: calls can be captured on `stream` (and the graph replayed)
  * once a call of the same shape has run eagerly on the same stream and
  * device: that call sets up the device and sizes the stream's workspace.  A
@@ -331,12 +333,12 @@ int sgemm_release_workspaces(void);
  * reserved up front by their own pool or by a host framework that forbids
  * later allocation, and latency-critical paths that cannot take an
  * allocation's cost or its possible synchronisation.  sgemm_noalloc runs the
- * same kernels, but keeps the transposed copy of A (and the split last
- * wave's partial tiles) in a fixed array compiled into the library (a
+ * same kernels, but keeps the transposed copy of A (and the partial tiles of
+ * the divided tail) in a fixed array compiled into the library (a
  * file-scope __device__ array of 16,777,216 floats, 64 MiB).  It calls no
  * cudaMalloc, cudaMallocAsync, cudaFree or other allocating routine.  Where
- * the array has no room for the partial tiles beside A^T, the last wave runs
- * unsplit, so the last bits can differ from sgemm()'s.
+ * the array has no room for the partial tiles beside A^T, the tail runs as
+ * whole tiles, so the last bits can differ from sgemm()'s.
  *
  * Limit: shapes sgemm() runs on its FFMA tile kernel (M > 16, B 16-byte
  * aligned, ldb % 4 == 0) need K * round_up(M, 4) <= 16,777,216 floats

@@ -326,7 +326,7 @@ def test_pair_tiles(mode, M, N, K):
 
 # ---------------------------------------------------------------- FFMA tile configurations
 # Every configuration compiled into the library (the autotuner's choices),
-# forced, on shapes with ragged edges, a split last wave and beta != 0.
+# forced, on shapes with ragged edges, a divided tail and beta != 0.
 @pytest.mark.parametrize("cfg", range(5))
 @pytest.mark.parametrize("M,N,K", [(300, 260, 516), (1500, 1100, 700), (129, 1000, 77),
                                    (2300, 2352, 1001), (31, 3000, 2050)])
@@ -346,12 +346,12 @@ def test_every_ffma_config(cfg, M, N, K):
 
 # ---------------------------------------------------------------- fused epilogue
 # C = act(alpha*A@B + beta*C + bias[j]) on every kernel path: the TMA tile
-# kernel (whole tiles and a split last wave), the plain-load kernel, the
+# kernel (whole tiles and a divided tail), the plain-load kernel, the
 # decode kernels (both outer-product tiles, the TMA and the direct-load
 # kernel), C = act(beta*C + bias) without the product, and the tensor-core
 # kernels on one-SM and two-SM tiles in all three arithmetics.
 EPI_CASES = [  # (M, N, K, kernel, tensor_cores, ldb padding, lda padding)
-    (300, 260, 516, TMA, False, 0, 0),        # 9 tiles, split along K
+    (300, 260, 516, TMA, False, 0, 0),        # 9 tiles, divided by work
     (1100, 700, 200, TMA, False, 0, 0),       # whole tiles
     (150, 130, 70, GEN, False, 3, 0),
     (16, 1000, 512, DEC, False, 0, 0),        # outer-product decode kernel, 16-row tile
@@ -557,9 +557,10 @@ def test_large_ragged_full_compare(M, N, K, beta):
     assert chosen == TMA
 
 
-# Shapes whose last wave is split along K (tiles over 304 resident blocks on
-# a 152-SM GB300: 1000^3 has 64 tiles in 4 parts each, 1500x1100x700 has 108
-# tiles in 2 parts); every output compared, and a second call is bitwise equal.
+# Shapes whose tail (the tiles after the last full wave of resident blocks,
+# all of them when they fill less than one wave) is divided by work into equal
+# runs of K iterations; every output compared, and a second call is bitwise
+# equal.
 @pytest.mark.parametrize("M,N,K,beta,ldc_pad", [(1000, 1000, 1000, 0.0, 0), (1500, 1100, 700, -0.4, 5),
                                                 (1001, 999, 513, 1.0, 3)])
 def test_split_last_wave(M, N, K, beta, ldc_pad):
@@ -578,7 +579,7 @@ def test_split_last_wave(M, N, K, beta, ldc_pad):
 
 
 # Skinny products, 17 <= M <= 128 (the band between the decode kernel and
-# full tiles: 32-row tiles, split along K so the few tiles fill the GPU);
+# full tiles: 32-row tiles, the tail divided by work so the few tiles fill the GPU);
 # ragged M, N and K, every output compared.
 SK_M = [17, 24, 31, 32, 33, 48, 63, 64, 65, 100, 127, 128]
 SK_NK = [(257, 100), (3001, 1031), (14336, 4096)]

@@ -10,10 +10,10 @@ C ABI and check:
   - its output against the fp64 oracle (the parity gate) and against sgemm(),
     the entry point that does allocate, on two calls in a row (the second
     call reuses the array the first one left behind);
-  - a problem that fills the array exactly, with a partial last wave: there
-    is no room for the split last wave's partial tiles, so the last wave runs
-    unsplit (a different summation order from sgemm()'s) and still meets the
-    gate;
+  - a problem that fills the array exactly and whose tiles fill less than
+    one wave: there is no room for the partial tiles of a divided tail, so the
+    tiles run whole (a different summation order from sgemm()'s) and still
+    meet the gate;
   - that a call allocates nothing: with every sgemm() workspace released,
     device free memory does not drop across a call, while the same call
     through sgemm() then takes memory for its workspace;
@@ -98,11 +98,12 @@ def test_matches_oracle_and_sgemm_on_two_calls_in_a_row(noalloc):
     _compare_one(noalloc, 300, 516, 260, -0.75, 0.0, seed=42)
 
 
-def test_full_array_runs_the_last_wave_unsplit(noalloc):
-    # M = K = 4096: A^T fills the array, so the partial tiles of a split last
-    # wave have no room.  At N = 512 the 4096 x 512 output is a few hundred
+def test_full_array_runs_the_tail_as_whole_tiles(noalloc):
+    # M = K = 4096: A^T fills the array, so the partial tiles of a divided
+    # tail have no room.  At N = 512 the 4096 x 512 output is a few hundred
     # tiles, less than one wave of resident CTAs, which sgemm() (whose
-    # workspace grows) splits along K; sgemm_noalloc must run it unsplit.
+    # workspace grows) divides by work along K; sgemm_noalloc must run the
+    # tiles whole.
     M = K = 4096
     assert K * M == ARRAY_FLOATS
     got, want = _compare_one(noalloc, M, 512, K, 1.0, 0.25, seed=43)
