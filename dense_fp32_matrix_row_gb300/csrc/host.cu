@@ -27,7 +27,10 @@ using namespace sgemm_gb300;
 namespace {
 
 constexpr int kSlots = 2;
-constexpr int kBParts = 4;   // most K-ranges B arrives in while the first panel computes
+#ifndef HOST_B_PARTS
+#define HOST_B_PARTS 4
+#endif
+constexpr int kBParts = HOST_B_PARTS;   // most K-ranges B arrives in while the first panel computes
 constexpr size_t kAlign = 256;   // bytes; every device sub-buffer starts on this boundary
 
 struct HostPath {
@@ -97,7 +100,7 @@ void destroy(HostPath &h) {
 int b_parts(int64_t M, int64_t rows, int64_t K, bool uses_ab) {
     if (!uses_ab || rows >= M) return 1;
     if (K >= 2048) return kBParts;
-    if (K >= 1024) return 2;
+    if (K >= 1024) return std::min(kBParts, 2);
     return 1;
 }
 
