@@ -58,7 +58,6 @@ MODES = {"fp32": lambda sg: sg.MODE_FP32, "3xtf32": lambda sg: sg.MODE_3XTF32,
 KERNEL_SOURCES = {
     "ffma_tma": ["dense_fp32_matrix_row_gb300/csrc/ffma_tma.cu",
                  "dense_fp32_matrix_row_gb300/csrc/ffma_tuning.inc",
-                 "dense_fp32_matrix_row_gb300/csrc/transpose.cu",
                  "dense_fp32_matrix_row_gb300/csrc/common.cuh"],
     "decode": ["dense_fp32_matrix_row_gb300/csrc/decode.cu",
                "dense_fp32_matrix_row_gb300/csrc/common.cuh"],

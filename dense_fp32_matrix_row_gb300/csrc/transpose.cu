@@ -99,30 +99,30 @@ transpose_tile_kernel(int64_t R, int64_t Cc, const float *__restrict__ src, int6
                 for (int e = 0; e < 4; ++e)
                     if (r + e < R) pb[e] = __float2bfloat16_rn(v[e]);
             }
-            continue;
-        }
-        float h[4], l[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (SPLIT) {
-                h[e] = tf32_rna(v[e]);
-                l[e] = tf32_rna(v[e] - h[e]);
-            } else {
-                h[e] = v[e];
-            }
-        }
-        float *ph = dst_hi + c * ldd + r;
-        const bool wlo = SPLIT && dst_lo != nullptr;
-        float *pl = wlo ? dst_lo + c * ldd + r : nullptr;
-        if (r + 3 < R) {
-            *reinterpret_cast<float4 *>(ph) = make_float4(h[0], h[1], h[2], h[3]);
-            if (wlo) *reinterpret_cast<float4 *>(pl) = make_float4(l[0], l[1], l[2], l[3]);
         } else {
+            float h[4], l[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (r + e < R) {
-                    ph[e] = h[e];
-                    if (wlo) pl[e] = l[e];
+                if (SPLIT) {
+                    h[e] = tf32_rna(v[e]);
+                    l[e] = tf32_rna(v[e] - h[e]);
+                } else {
+                    h[e] = v[e];
+                }
+            }
+            float *ph = dst_hi + c * ldd + r;
+            const bool wlo = SPLIT && dst_lo != nullptr;
+            float *pl = wlo ? dst_lo + c * ldd + r : nullptr;
+            if (r + 3 < R) {
+                *reinterpret_cast<float4 *>(ph) = make_float4(h[0], h[1], h[2], h[3]);
+                if (wlo) *reinterpret_cast<float4 *>(pl) = make_float4(l[0], l[1], l[2], l[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (r + e < R) {
+                        ph[e] = h[e];
+                        if (wlo) pl[e] = l[e];
+                    }
                 }
             }
         }
