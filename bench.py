@@ -338,7 +338,10 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
     "ms_eager" per call with an event pair around each eager call."""
     import synth
     out = {}
+    # the FP32 FFMA peak (SMs x 128 lanes x 2 FLOP x max clock), and the
     # measured bf16 x the nominal TF32 / BF16 ratio, burst and sustained
+    ffma_peak = (torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2
+                 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12)
     tf32_peak = peaks["bf16_tflops"] * 1.1 / 2.25
     tf32_peak_s = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1.1 / 2.25
     tf32_peak = peaks["bf16_tflops"] * 1.1 / 2.25   # measured bf16 x nominal tf32/bf16
@@ -471,15 +474,11 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
 
     # skinny products, 17 <= M <= 128 rows on the decode shapes' N and K (the
     # same B): HBM-bound below about 24 rows, FFMA-bound above
-    ffma_peak = None
     for M in (32, 64, 128):
         A, B, C0, w = synth.workload_inputs(f"skinny_m{M}")
         N, K = w["N"], w["K"]
         r = bench_shape(A, B, C0, w["alpha"], w["beta"], rotate=3)
         nbytes = 4 * (M * K + K * N + M * N)
-        if ffma_peak is None:
-            props = torch.cuda.get_device_properties(dev)
-            ffma_peak = props.multi_processor_count * 128 * 2 * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
         t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e3
         t_alu = 2.0 * M * N * K / (ffma_peak * 1e12) * 1e3
         r["TFLOP/s"] = tflops(r, M, N, K)
@@ -498,11 +497,13 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
         M, N, K = w["M"], w["N"], w["K"]
         r = bench_shape(A, B, C0, w["alpha"], w["beta"])
         r["TFLOP/s"] = tflops(r, M, N, K)
+        r["frac_ffma_peak"] = r["TFLOP/s"] / ffma_peak
         out[name] = r
         if name == "prefill_up":
             # FFN-up with the fused epilogue act(X W + bias), SiLU
             r = bench_shape(A, B, C0, w["alpha"], w["beta"], activation="silu", bias_seed=w["seed"])
             r["TFLOP/s"] = tflops(r, M, N, K)
+            r["frac_ffma_peak"] = r["TFLOP/s"] / ffma_peak
             r["epilogue"] = "bias + SiLU (sgemm_fused)"
             out["prefill_up_bias_silu"] = r
         if name == "sgemm_8192":
@@ -546,6 +547,7 @@ def secondary(sg, torch, stream, dev, peaks, steps=20, warmup=3, check=True):
         B = synth.matrix(K, N, seed=10 + i, stream=1, dist="normal")
         r = bench_shape(A, B, None, 1.0, 0.0)
         r["TFLOP/s"] = tflops(r, M, N, K)
+        r["frac_ffma_peak"] = r["TFLOP/s"] / ffma_peak
         r["l2_resident"] = True
         r["data"] = f"A, B normal(0,1), seed {10 + i}"
         out[name] = r
