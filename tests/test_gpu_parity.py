@@ -70,6 +70,17 @@ def test_decode_shapes(M, N, K):
     assert chosen == DEC
 
 
+# The outer-product tile with M = 9..16 rows and long K: clusters of up to
+# 16 blocks (non-portable sizes), ragged last K slices, integer data so that
+# any misplaced or dropped k-step shows exactly.
+@pytest.mark.parametrize("M,K", [(9, 436), (16, 3364), (12, 6720), (16, 6724), (13, 8192)])
+def test_decode_slice_limits(M, K):
+    N = 300
+    A, B, C0 = make_inputs(M, N, K, "int", seed=M + K, beta=-2.0)
+    _, chosen = run_checked(sg, A, B, C0, 3.0, -2.0, exact=True)
+    assert chosen == DEC
+
+
 # ---------------------------------------------------------------- exactness
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (4, 14336, 4096), (300, 200, 1000),
                                    (16, 129, 5000)])
