@@ -448,6 +448,16 @@ __device__ __forceinline__ void fma_row8(float (&acc)[8], float a, const float (
 //
 // After the K loop the k groups' partial tiles are summed in a fixed order
 // in shared memory, then across the cluster.
+//
+// The kernel is launched as a programmatic dependent of whatever precedes it
+// on the stream: its blocks may become resident and initialise their
+// barriers while that work finishes, and wait (pdl_wait) before the first
+// copy.  Once past its K loop a block lets the next such kernel launch, so
+// back-to-back decode products (a model's layers) overlap one kernel's
+// reduction with the next one's launch.
+#ifndef DECODE_PDL
+#define DECODE_PDL 1   // programmatic dependent launch of the outer-product tile
+#endif
 #ifndef DECODE_DO_TKB
 #define DECODE_DO_TKB 16   // k-steps per TMA stage
 #endif
@@ -551,12 +561,19 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
         }
         mbar_fence_init();
     }
-    __syncthreads();
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmA);
-        for (int st = 0; st < DO_STAGES && st < nst; ++st) issue(st);
     }
+#if DECODE_PDL
+    // Launched as a programmatic dependent of the work before it on the
+    // stream: everything above overlaps that work's tail; A, B and C are
+    // touched only after it has completed.
+    pdl_wait();
+#endif
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int st = 0; st < DO_STAGES && st < nst; ++st) issue(st);
 
     float acc[MTL][8];
 #pragma unroll
@@ -635,6 +652,11 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
 
     if (threadIdx.x == 0) drain();
     const bool any_failed = __syncthreads_or(failed) != 0;
+#if DECODE_PDL
+    // the next kernel on the stream may launch once every block is here (it
+    // waits for this grid to complete before touching memory)
+    pdl_trigger();
+#endif
     // k-group partials to shared memory (the ring is free now), then their
     // sum in k-group order into group 0's slot.
 #pragma unroll
@@ -842,13 +864,15 @@ cudaError_t launch_outer(const GemmArgs &g) {
     kslice = (kslice + DO_TKB - 1) / DO_TKB * DO_TKB;
 
     cfg.gridDim = dim3((unsigned)ks, (unsigned)ncb, 1);
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)ks;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = DECODE_PDL;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, tmB, tmA, (int)g.M, (int64_t)g.N, (int64_t)g.K, g.epi(),
                               g.C, g.ldc, kslice, g.err, g.wait_ns);
 }

@@ -81,3 +81,57 @@ def test_capture_refuses_to_grow_the_workspace():
         with torch.cuda.graph(g, stream=s):
             sg.sgemm(big_A, big_B, big_C, 1.0, 0.0, stream=s)
     assert ei.value.code == sg.ERR_CAPTURE
+
+
+@pytest.mark.parametrize("captured", [False, True])
+def test_chained_decode_products_see_each_others_results(captured):
+    # Each decode kernel may become resident while the kernel before it on
+    # the stream is still running and waits for it before its first copy.
+    # Chains C1 = A0 B1, C2 = C1 B2 (the second product reads the first one's
+    # output as A), repeated back to back with C1 and C2 reset to NaN before
+    # each chain: a product that read its A too early would see NaN.  Small
+    # integers keep every sum exact, so each link must match the oracle's
+    # chain bit for bit.
+    M, K0, K1, N = 16, 4096, 512, 4096
+    rng = np.random.default_rng(61)
+    A0 = rng.integers(-1, 2, (M, K0)).astype(np.float32)
+    B1 = rng.integers(-1, 2, (K0, K1)).astype(np.float32)
+    B2 = rng.integers(-1, 2, (K1, N)).astype(np.float32)
+    C1_ref = oracle.sgemm(A0, B1, alpha=1.0, beta=0.0)
+    C2_ref = oracle.sgemm(C1_ref.astype(np.float32), B2, alpha=1.0, beta=0.0)
+    assert np.abs(C2_ref).max() < 2 ** 24
+    s = torch.cuda.Stream()
+    dA0, dB1, dB2 = (torch.from_numpy(x).cuda() for x in (A0, B1, B2))
+    chains = 6
+    C1 = [torch.empty((M, K1), device="cuda") for _ in range(chains)]
+    C2 = [torch.empty((M, N), device="cuda") for _ in range(chains)]
+    assert sg.select_kernel(M, K1, K0, 1.0, dA0.data_ptr(), K0, dB1.data_ptr(), K1, 0.0,
+                            C1[0].data_ptr(), K1) == sg.KERNEL_DECODE
+    assert sg.select_kernel(M, N, K1, 1.0, C1[0].data_ptr(), K1, dB2.data_ptr(), N, 0.0,
+                            C2[0].data_ptr(), N) == sg.KERNEL_DECODE
+
+    def run():
+        for i in range(chains):
+            sg.sgemm(dA0, dB1, C1[i], 1.0, 0.0, stream=s)
+            sg.sgemm(C1[i], dB2, C2[i], 1.0, 0.0, stream=s)
+
+    with torch.cuda.stream(s):
+        run()                                  # set-up calls
+    s.synchronize()
+    for t in C1 + C2:
+        t.fill_(float("nan"))
+    torch.cuda.synchronize()
+    if captured:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            run()
+        with torch.cuda.stream(s):
+            g.replay()
+    else:
+        with torch.cuda.stream(s):
+            run()
+    s.synchronize()
+    assert sg.status(s) == sg.OK
+    for i in range(chains):
+        assert np.array_equal(C1[i].cpu().numpy(), C1_ref.astype(np.float32)), f"chain {i}: C1"
+        assert np.array_equal(C2[i].cpu().numpy(), C2_ref.astype(np.float32)), f"chain {i}: C2"
