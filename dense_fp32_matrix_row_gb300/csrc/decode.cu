@@ -463,7 +463,10 @@ __device__ __forceinline__ void fma_row8(float (&acc)[8], float a, const float (
 #endif
 constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32, DO_TKB = DECODE_DO_TKB;
 #ifndef DECODE_DO_STAGES
-#define DECODE_DO_STAGES 2
+#define DECODE_DO_STAGES 2      // TMA stages of the 8-row tile
+#endif
+#ifndef DECODE_DO_STAGES_16
+#define DECODE_DO_STAGES_16 3   // TMA stages of the 16-row tile
 #endif
 #ifndef DECODE_DO_MINB
 #define DECODE_DO_MINB 0   // blocks per SM the registers are sized for; 0: by row count
@@ -471,7 +474,6 @@ constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32, DO_TKB = 
 #ifndef DECODE_DO_KS
 #define DECODE_DO_KS 0
 #endif
-constexpr int DO_STAGES = DECODE_DO_STAGES;
 #ifndef DECODE_AT
 #define DECODE_AT 0
 #endif
@@ -485,13 +487,17 @@ struct DoCfg {
     // 64 accumulators per lane at MT/RG = 8: five blocks per SM (96 registers)
     // suit M <= 8; at M = 16, four blocks (128 registers) measured faster.
     static constexpr int MINB = DECODE_DO_MINB > 0 ? DECODE_DO_MINB : (MT <= 8 ? 5 : 4);
+    // Stages: at four blocks per SM the 16-row tile has room for a third
+    // (measured 4.82 -> 4.98 TB/s at M = 16); a third stage would cost the
+    // 8-row tile its fifth block (5.99 -> 5.48 at M = 8).
+    static constexpr int STAGES = MT > 8 ? DECODE_DO_STAGES_16 : DECODE_DO_STAGES;
     static constexpr int KG = DO_WARPS / RG;                               // k groups
     static constexpr int MTL = MT / RG;                                    // rows per lane
     static constexpr int RPW = DO_TKB / KG;                                // k-steps per warp per stage
     static constexpr size_t B_PANEL = (size_t)DO_TKB * DO_COLS;            // floats, [k][n]
     static constexpr size_t A_PANEL = (size_t)MT * DO_TKB;                 // floats, [m][k]
     static constexpr size_t STAGE = B_PANEL + A_PANEL;
-    static constexpr size_t RING = DO_STAGES * STAGE;
+    static constexpr size_t RING = STAGES * STAGE;
     static constexpr size_t RED = (size_t)KG * MT * DO_COLS;              // aliases the ring
     static constexpr size_t REGION0 = RING > RED ? RING : RED;
     // The 16-row tile: each warp transposes its A values of a stage to [k][m]
@@ -501,7 +507,7 @@ struct DoCfg {
     static constexpr bool TRANSPOSE_A = MT > 8 ? DECODE_AT_16 : DECODE_AT;
     static constexpr bool PACKED = MT > 8 ? DECODE_PACKED_16 : DECODE_PACKED;
     static constexpr size_t AT = TRANSPOSE_A ? (size_t)DO_WARPS * RPW * MTL : 0;   // [warp][k][m]
-    static constexpr size_t BYTES = 128 + (REGION0 + AT) * 4 + DO_STAGES * 16;
+    static constexpr size_t BYTES = 128 + (REGION0 + AT) * 4 + STAGES * 16;
     static_assert(DO_WARPS % RG == 0 && MT % RG == 0 && DO_TKB % KG == 0, "warp split");
     static_assert(!TRANSPOSE_A || (RPW * MTL) % 32 == 0, "whole lanes in the A transpose");
     static_assert(MTL % 4 == 0, "A rows come in float4 groups");
@@ -515,11 +521,11 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
                     int M, int64_t N, int64_t K, Epilogue ep, float *__restrict__ C,
                     int64_t ldc, int64_t kslice, unsigned *err, uint64_t wait_ns) {
     using L = DoCfg<MT, RG>;
-    constexpr int KG = L::KG, MTL = L::MTL;
+    constexpr int KG = L::KG, MTL = L::MTL, DO_STAGES = L::STAGES;
     extern __shared__ unsigned char smem_raw[];
     float *smem = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                             ~uintptr_t(127));
-    float *ring = smem;                    // [DO_STAGES][B panel | A panel]
+    float *ring = smem;                    // [STAGES][B panel | A panel]
     float *red = smem;                     // [KG][MT][DO_COLS], after the K loop
     float *at = smem + L::REGION0 + (size_t)(threadIdx.x >> 5) * L::RPW * MTL;   // this warp's A^T
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::REGION0 + L::AT);
