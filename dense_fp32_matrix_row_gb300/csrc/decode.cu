@@ -430,8 +430,8 @@ __device__ __forceinline__ void fma_row8(float (&acc)[8], float a, const float (
 
 // ---------------------------------------------------------------- outer-product variant (M >= 5)
 // A block owns an MT x 256 tile of C.  Each stage of its TMA ring carries
-// both operands of DO_TKB k-steps: the DO_TKB x 256 panel of B ([k][n]) and
-// the MT x DO_TKB panel of A ([m][k], rows past M zero-filled by the copy),
+// both operands of TKB k-steps: the TKB x 256 panel of B ([k][n]) and
+// the MT x TKB panel of A ([m][k], rows past M zero-filled by the copy),
 // so the K loop has no block barrier and no global load of its own.  Needs
 // A and B 16-byte aligned with lda % 4 == 0 and ldb % 4 == 0.
 //
@@ -459,9 +459,12 @@ __device__ __forceinline__ void fma_row8(float (&acc)[8], float a, const float (
 #define DECODE_PDL 1   // programmatic dependent launch of the outer-product tile
 #endif
 #ifndef DECODE_DO_TKB
-#define DECODE_DO_TKB 16   // k-steps per TMA stage
+#define DECODE_DO_TKB 16      // k-steps per TMA stage, 8-row tile
 #endif
-constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32, DO_TKB = DECODE_DO_TKB;
+#ifndef DECODE_DO_TKB_16
+#define DECODE_DO_TKB_16 16   // k-steps per TMA stage, 16-row tile
+#endif
+constexpr int DO_COLS = 256, DO_WARPS = 4, DO_THREADS = DO_WARPS * 32;
 #ifndef DECODE_DO_STAGES
 #define DECODE_DO_STAGES 2      // TMA stages of the 8-row tile
 #endif
@@ -491,11 +494,12 @@ struct DoCfg {
     // (measured 4.82 -> 4.98 TB/s at M = 16); a third stage would cost the
     // 8-row tile its fifth block (5.99 -> 5.48 at M = 8).
     static constexpr int STAGES = MT > 8 ? DECODE_DO_STAGES_16 : DECODE_DO_STAGES;
+    static constexpr int TKB = MT > 8 ? DECODE_DO_TKB_16 : DECODE_DO_TKB;   // a multiple of 4 (TMA x)
     static constexpr int KG = DO_WARPS / RG;                               // k groups
     static constexpr int MTL = MT / RG;                                    // rows per lane
-    static constexpr int RPW = DO_TKB / KG;                                // k-steps per warp per stage
-    static constexpr size_t B_PANEL = (size_t)DO_TKB * DO_COLS;            // floats, [k][n]
-    static constexpr size_t A_PANEL = (size_t)MT * DO_TKB;                 // floats, [m][k]
+    static constexpr int RPW = TKB / KG;                                // k-steps per warp per stage
+    static constexpr size_t B_PANEL = (size_t)TKB * DO_COLS;            // floats, [k][n]
+    static constexpr size_t A_PANEL = (size_t)MT * TKB;                 // floats, [m][k]
     static constexpr size_t STAGE = B_PANEL + A_PANEL;
     static constexpr size_t RING = STAGES * STAGE;
     static constexpr size_t RED = (size_t)KG * MT * DO_COLS;              // aliases the ring
@@ -508,7 +512,7 @@ struct DoCfg {
     static constexpr bool PACKED = MT > 8 ? DECODE_PACKED_16 : DECODE_PACKED;
     static constexpr size_t AT = TRANSPOSE_A ? (size_t)DO_WARPS * RPW * MTL : 0;   // [warp][k][m]
     static constexpr size_t BYTES = 128 + (REGION0 + AT) * 4 + STAGES * 16;
-    static_assert(DO_WARPS % RG == 0 && MT % RG == 0 && DO_TKB % KG == 0, "warp split");
+    static_assert(DO_WARPS % RG == 0 && MT % RG == 0 && TKB % KG == 0 && TKB % 4 == 0, "warp split");
     static_assert(!TRANSPOSE_A || (RPW * MTL) % 32 == 0, "whole lanes in the A transpose");
     static_assert(MTL % 4 == 0, "A rows come in float4 groups");
     static_assert((STAGE * 4) % 128 == 0, "stage offsets stay 128-byte aligned");
@@ -521,7 +525,7 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
                     int M, int64_t N, int64_t K, Epilogue ep, float *__restrict__ C,
                     int64_t ldc, int64_t kslice, unsigned *err, uint64_t wait_ns) {
     using L = DoCfg<MT, RG>;
-    constexpr int KG = L::KG, MTL = L::MTL, DO_STAGES = L::STAGES;
+    constexpr int KG = L::KG, MTL = L::MTL, DO_STAGES = L::STAGES, TKB = L::TKB;
     extern __shared__ unsigned char smem_raw[];
     float *smem = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                             ~uintptr_t(127));
@@ -540,13 +544,13 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
     const int64_t n0 = (int64_t)blockIdx.y * DO_COLS;
     const int64_t kbeg = (int64_t)rank * kslice;
     const int64_t kend = (kbeg + kslice < K) ? kbeg + kslice : K;
-    const int nst = kend > kbeg ? (int)((kend - kbeg + DO_TKB - 1) / DO_TKB) : 0;
+    const int nst = kend > kbeg ? (int)((kend - kbeg + TKB - 1) / TKB) : 0;
 
     auto issue = [&](int st) {
         const int s = st % DO_STAGES;
         issued[s] = st;
         const uint32_t fb = smem_u32(&full[s]);
-        const int32_t kc = (int32_t)(kbeg + (int64_t)st * DO_TKB);
+        const int32_t kc = (int32_t)(kbeg + (int64_t)st * TKB);
         float *stg = ring + s * L::STAGE;
         mbar_arrive_expect_tx(fb, (uint32_t)(L::STAGE * 4));
         tma_load_2d(smem_u32(stg), &tmB, fb, (int32_t)n0, kc);
@@ -600,14 +604,14 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
         }
         const float *stg = ring + s * L::STAGE;
         const float *bst = stg + lane * 4;
-        const float *ast = stg + L::B_PANEL + (size_t)rg * MTL * DO_TKB;
+        const float *ast = stg + L::B_PANEL + (size_t)rg * MTL * TKB;
         if constexpr (L::TRANSPOSE_A) {
             // this warp's A values of the stage, transposed to [k][m] so that
             // a k-step's MTL values are float4 loads
 #pragma unroll
             for (int e = lane; e < L::RPW * MTL; e += 32) {
                 const int rr = e / MTL, m = e % MTL;
-                at[e] = ast[m * DO_TKB + kg + KG * rr];
+                at[e] = ast[m * TKB + kg + KG * rr];
             }
             __syncwarp();
         }
@@ -632,7 +636,7 @@ decode_outer_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_consta
             } else {
 #pragma unroll
                 for (int m = 0; m < MTL; ++m)
-                    fma_row8<L::PACKED>(acc[m], ast[m * DO_TKB + r], bv, m & 1);
+                    fma_row8<L::PACKED>(acc[m], ast[m * TKB + r], bv, m & 1);
             }
         }
         if constexpr (L::TRANSPOSE_A) __syncwarp();   // lanes are done with `at` before it is rewritten
@@ -845,9 +849,9 @@ cudaError_t launch_outer(const GemmArgs &g) {
     using L = DoCfg<MT, RG>;
     static std::atomic<int> cache[64][17];
     alignas(64) CUtensorMap tmB, tmA;
-    if (!encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, DO_COLS, DO_TKB, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_tma_2d(g.encode, &tmB, g.B, g.N, g.K, g.ldb, DO_COLS, L::TKB, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    if (!encode_tma_2d(g.encode, &tmA, g.A, g.K, g.M, g.lda, DO_TKB, MT, CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_tma_2d(g.encode, &tmA, g.A, g.K, g.M, g.lda, L::TKB, MT, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     auto kern = decode_outer_kernel<MT, RG>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
@@ -864,10 +868,10 @@ cudaError_t launch_outer(const GemmArgs &g) {
     cfg.blockDim = dim3(DO_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::BYTES;
     cfg.stream = g.stream;
-    int ks = choose_cluster(kern, g.K, ncb, ksmax, DO_TKB, cfg, cache);
-    if (DECODE_DO_KS > 0 && g.K >= (int64_t)DECODE_DO_KS * DO_TKB) ks = DECODE_DO_KS;
+    int ks = choose_cluster(kern, g.K, ncb, ksmax, L::TKB, cfg, cache);
+    if (DECODE_DO_KS > 0 && g.K >= (int64_t)DECODE_DO_KS * L::TKB) ks = DECODE_DO_KS;
     int64_t kslice = (g.K + ks - 1) / ks;
-    kslice = (kslice + DO_TKB - 1) / DO_TKB * DO_TKB;
+    kslice = (kslice + L::TKB - 1) / L::TKB * L::TKB;
 
     cfg.gridDim = dim3((unsigned)ks, (unsigned)ncb, 1);
     cudaLaunchAttribute attr[2];
