@@ -686,6 +686,12 @@ def run_ours(args, world, rank, local):
             peak_source = "measured bf16 GEMM burst x 1.1/2.25 (nominal TF32/BF16 ratio)"
         if kid == sg.KERNEL_TF32X3:
             achieved *= 3      # three TF32 products per useful product
+    unit = "TFLOP/s"
+    if kid == sg.KERNEL_DECODE:
+        # M <= 16: bound by streaming B, measured against the copy bandwidth
+        bound, unit = "hbm", "GB/s"
+        achieved = acc.min_traffic_bytes(M, N, K, beta != 0.0) / (per_launch_ms * 1e-3) / 1e9
+        peak, peak_source = peaks["hbm_gbs"], "measured HBM copy bandwidth"
     traffic = ncu_traffic("ffma_tma", name) if kid == sg.KERNEL_FFMA_TMA else None
     cpu = None
     if not args.no_cpu_baseline:
@@ -706,7 +712,7 @@ def run_ours(args, world, rank, local):
             "kernel": sg.KERNEL_NAMES.get(kid, str(kid)),
             "l2": f"operands {4 * (M * K + K * N + M * N) / 1e6:.0f} MB > L2 129 MB; no flush",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}),
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_source,
                      "kernel": ("transpose_tile_kernel<0> + ffma_tma_kernel, timed together as one sgemm() "
                                 "call; traffic is ffma_tma_kernel's alone"
