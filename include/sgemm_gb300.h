@@ -115,6 +115,11 @@ extern "C" {
  * 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section "10", applied to the tail
  * only).  The result is deterministic: the same inputs give the same bits on
  * every call on the same GPU model.
+ * Stream order: the decode kernel, and the FFMA kernel behind its transpose,
+ * are launched as programmatic dependents of the work before them on
+ * `stream`: their blocks may start their set-up while that work finishes,
+ * and wait for it to complete before touching A, B or C.  The decode kernel
+ * lets the next such launch start once its blocks are past their K loop.
  * CUDA graphs: calls can be captured on `stream` (and the graph replayed)
  * once a call of the same shape has run eagerly on the same stream and
  * device: that call sets up the device and sizes the stream's workspace.  A
