@@ -581,10 +581,13 @@ def run_ours(args, world, rank, local):
     tc = MODES[mode_name](sg)
     kid = sg.select_kernel(M, N, K, alpha, dA.data_ptr(), K, dB.data_ptr(), N, beta,
                            dC.data_ptr(), N, tc)
-    # kernels one sgemm() call launches: the FFMA path transposes A first, the
-    # tensor-core paths convert A and B first
+    # kernels one sgemm() call launches: the FFMA path transposes A first (and
+    # sums a divided tail in a kernel of its own), the tensor-core paths
+    # convert A and B first
     launches_per_call = {sg.KERNEL_FFMA_TMA: 2, sg.KERNEL_TF32X3: 3, sg.KERNEL_TF32: 3,
                          sg.KERNEL_BF16: 3}.get(kid, 1)
+    if kid == sg.KERNEL_FFMA_TMA:
+        launches_per_call += sg.ffma_tail_plan(M, N, K)["tail_sum"]
 
     def step():
         sg.sgemm(dA, dB, dC, alpha, beta, stream=stream, tensor_cores=tc)

@@ -16,7 +16,7 @@ import os
 from .build import LIBRARY, build  # noqa: F401  (build is part of the public API)
 
 __all__ = ["sgemm", "sgemm_host", "host_set_panels", "host_panel_rows", "sgemm_3xtf32", "sgemm_tf32", "sgemm_bf16", "sgemm_ptr", "status", "select_kernel",
-           "force_kernel", "ffma_configs", "ffma_config_for", "ffma_force_config", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
+           "force_kernel", "ffma_configs", "ffma_config_for", "ffma_force_config", "ffma_force_tail_sum", "ffma_tail_plan", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
            "version", "SgemmError", "lib"]
 
 OK = 0
@@ -288,6 +288,26 @@ def ffma_config_for(M: int, N: int) -> int:
 def ffma_force_config(idx: int) -> int:
     """Force FFMA tile configuration ``idx`` (-1: the tuning table); returns the previous."""
     return int(lib().sgemm_ffma_force_config(int(idx)))
+
+
+def ffma_force_tail_sum(mode: int) -> int:
+    """How a divided tail's partial tiles are summed (-1 the library's rule,
+    0 by the last unit to reach each tile, 1 by a separate kernel); returns
+    the previous setting."""
+    return int(lib().sgemm_ffma_force_tail_sum(int(mode)))
+
+
+def ffma_tail_plan(M: int, N: int, K: int) -> dict:
+    """The work list an FFMA-path sgemm() call of this shape runs on the
+    current device: units (CTAs), span (k-tiles per unit of the divided tail,
+    0 if not divided) and tail_sum (1: a separate kernel sums the tail)."""
+    units, span, ts = ctypes.c_int64(), ctypes.c_int(), ctypes.c_int()
+    f = lib().sgemm_ffma_tail_plan
+    f.argtypes = [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 3
+    rc = f(int(M), int(N), int(K), ctypes.addressof(units), ctypes.addressof(span), ctypes.addressof(ts))
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_ffma_tail_plan")
+    return {"units": units.value, "span": span.value, "tail_sum": ts.value}
 
 
 def set_wait_limit(ns: int) -> int:

@@ -468,6 +468,25 @@ int sgemm_ffma_force_config(int idx) {
     return prev == -2 ? SGEMM_ERR_BAD_ARG : prev;
 }
 
+int sgemm_ffma_force_tail_sum(int mode) {
+    const int prev = ffma_force_tail_sum(mode);
+    return prev == -2 ? SGEMM_ERR_BAD_ARG : prev;
+}
+
+int sgemm_ffma_tail_plan(int64_t M, int64_t N, int64_t K, int64_t *units, int *span, int *tail_sum) {
+    if (!units || !span || !tail_sum) return SGEMM_ERR_BAD_ARG;
+    if (M < 1 || N < 1 || K < 1 || M > ffma_tma_max_m() || N > INT32_MAX || K > INT32_MAX)
+        return SGEMM_ERR_BAD_DIM;
+    GemmArgs g{};
+    const int rc = fill_device_args(g);
+    if (rc != SGEMM_OK) return rc;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    ffma_tma_plan_info(g, units, span, tail_sum);
+    return SGEMM_OK;
+}
+
 int sgemm_version(void) { return 100; }
 
 }  // extern "C"

@@ -74,6 +74,11 @@ int64_t ffma_tma_workspace_floats(const GemmArgs &g, int64_t capacity);
 int ffma_config_for(int64_t M, int64_t N);
 int ffma_config_count();
 int ffma_force_config(int idx);
+int ffma_force_tail_sum(int mode);   // -1 default, 0 last arriver, 1 separate kernel; -2 if invalid
+// The work list an sgemm() call of g's shape runs on the FFMA-TMA path:
+// units (CTAs), span (k-tiles per tail unit, 0 when the tail is not
+// divided) and whether a separate kernel sums the tail (1) or not (0).
+void ffma_tma_plan_info(const GemmArgs &g, int64_t *units, int *span, int *tail_sum);
 bool ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *threads, int *minb);
 int64_t ffma_tma_at_ld(int64_t M);
 // Largest M the TMA FFMA kernel's grid can cover.

@@ -32,7 +32,7 @@
 //    CTA slots, then the tail divided by work -- equal runs of k-tile
 //    iterations, summed through partial tiles in a fixed order (the split-K
 //    of "CUDA 矩阵乘法优化：从朴素 Kernel 到接近 cuBLAS", section "10", see
-//    TailPlan and plan_units);
+//    TailPlan and plan_units) by a second kernel over all tail tiles;
 //  * the kernel is launched as a programmatic dependent of the transpose that
 //    writes its A^T, so its set-up overlaps the transpose's tail.
 //
@@ -134,6 +134,7 @@ struct FfmaTuneEntry {
 #include "ffma_tuning.inc"
 
 std::atomic<int> g_force_config{-1};
+std::atomic<int> g_force_tail_sum{-1};   // sgemm_ffma_force_tail_sum
 
 __device__ __forceinline__ float comp(const float4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -241,7 +242,11 @@ __device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int
 // `partials` and counts the tile's arrival in counters[tile - full] (zeroed
 // before the launch); the unit that completes the count sums the tile's
 // partial tiles in unit order and runs the epilogue.  No unit waits for
-// another, and the sum order does not depend on timing.
+// another, and the sum order does not depend on timing.  By default the
+// units only write their partial tiles and ffma_tail_reduce_kernel, launched
+// right after the tile kernel, sums every tile's partials in the same order
+// (reduce_pass); the in-kernel sum by the last unit to arrive remains
+// selectable (sgemm_ffma_force_tail_sum) and gives the same bits.
 struct TailPlan {
     int tiles_x;
     int full;             // whole-tile units
@@ -249,6 +254,8 @@ struct TailPlan {
     int tail_iters;       // rem * ktiles
     float *partials;      // two slots per tail unit, each [TM * TN / 4][THREADS] float4
     unsigned *counters;   // [rem]
+    int reduce_pass;      // 1: every tail unit only writes its partial tiles; a second
+                          // kernel (ffma_tail_reduce_kernel) sums them
 };
 
 // Slot of tail unit v's partial tile of tail tile t: 2v + 1 when v's run ends
@@ -402,34 +409,37 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
                     __stcg(mine + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x,
                            make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2],
                                        acc[i][4 * h + 3]));
-            __threadfence();
-            __syncthreads();
-            if (threadIdx.x == 0) s_prev = atomicAdd(&tp.counters[t], 1u);
-            __syncthreads();
-            const int v0 = t * ktiles / tp.span, v1 = ((t + 1) * ktiles - 1) / tp.span;
-            if (s_prev == (unsigned)(v1 - v0)) {
-                // last one in: sum the partial tiles of units v0 .. v1 in that
-                // order (this unit's included), whichever unit arrived last
+            // with a reduce pass the partial tile is all this unit contributes
+            if (!tp.reduce_pass) {
                 __threadfence();
-                for (int w = v0; w <= v1; ++w) {
-                    const float4 *src = reinterpret_cast<const float4 *>(tp.partials) +
-                                        (size_t)partial_slot(w, t, tp.span, ktiles, tp.tail_iters) * NV *
-                                            C::THREADS;
+                __syncthreads();
+                if (threadIdx.x == 0) s_prev = atomicAdd(&tp.counters[t], 1u);
+                __syncthreads();
+                const int v0 = t * ktiles / tp.span, v1 = ((t + 1) * ktiles - 1) / tp.span;
+                if (s_prev == (unsigned)(v1 - v0)) {
+                    // last one in: sum the partial tiles of units v0 .. v1 in that
+                    // order (this unit's included), whichever unit arrived last
+                    __threadfence();
+                    for (int w = v0; w <= v1; ++w) {
+                        const float4 *src = reinterpret_cast<const float4 *>(tp.partials) +
+                                            (size_t)partial_slot(w, t, tp.span, ktiles, tp.tail_iters) * NV *
+                                                C::THREADS;
 #pragma unroll
-                    for (int i = 0; i < TM; ++i)
+                        for (int i = 0; i < TM; ++i)
 #pragma unroll
-                        for (int h = 0; h < TN / 4; ++h) {
-                            const float4 q = __ldcg(src + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x);
-                            if (w == v0) {
-                                acc[i][4 * h] = q.x; acc[i][4 * h + 1] = q.y;
-                                acc[i][4 * h + 2] = q.z; acc[i][4 * h + 3] = q.w;
-                            } else {
-                                acc[i][4 * h] += q.x; acc[i][4 * h + 1] += q.y;
-                                acc[i][4 * h + 2] += q.z; acc[i][4 * h + 3] += q.w;
+                            for (int h = 0; h < TN / 4; ++h) {
+                                const float4 q = __ldcg(src + (size_t)(i * (TN / 4) + h) * C::THREADS + threadIdx.x);
+                                if (w == v0) {
+                                    acc[i][4 * h] = q.x; acc[i][4 * h + 1] = q.y;
+                                    acc[i][4 * h + 2] = q.z; acc[i][4 * h + 3] = q.w;
+                                } else {
+                                    acc[i][4 * h] += q.x; acc[i][4 * h + 1] += q.y;
+                                    acc[i][4 * h + 2] += q.z; acc[i][4 * h + 3] += q.w;
+                                }
                             }
-                        }
+                    }
+                    store_tile<C>(acc, m0, n0, arow, bcol, M, N, ep, Cm, ldc, c_vec4);
                 }
-                store_tile<C>(acc, m0, n0, arow, bcol, M, N, ep, Cm, ldc, c_vec4);
             }
         }
         j0 = j1;
@@ -442,6 +452,69 @@ ffma_tma_kernel(const __grid_constant__ CUtensorMap tmAt, const __grid_constant_
     }
     // Every warp is past its k loop, so `issued` no longer changes.
     if (any_failed && threadIdx.x == 0) drain();
+}
+
+// The tail's partial tiles summed by a kernel of their own (TailPlan::
+// reduce_pass): one thread per float4 of a tail tile, the partials of units
+// v0 .. v1 added in that order and the epilogue applied -- the same
+// arithmetic, in the same order, as the last unit to arrive would do, spread
+// over the whole GPU instead of one CTA per tile.  Launched as a
+// programmatic dependent of the tile kernel.
+template <class C>
+__global__ void __launch_bounds__(256)
+ffma_tail_reduce_kernel(TailPlan tp, int ktiles, int M, int N, Epilogue ep, float *__restrict__ Cm,
+                        int64_t ldc, int c_vec4) {
+    constexpr int TM = C::TM, TN = C::TN, NV = TM * TN / 4;
+    constexpr int PER_TILE = NV * C::THREADS;   // float4s of one partial tile
+    pdl_wait();
+    const int t = blockIdx.y;                   // tail tile
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= PER_TILE) return;
+    // the tile kernel's thread (tid) and register (i, h) this float4 came from
+    const int tid = e % C::THREADS, q = e / C::THREADS;
+    const int i = q / (TN / 4), h = q % (TN / 4);
+    const int warp = tid >> 5, lane = tid & 31;
+    const int wm = warp / C::WN, wn = warp % C::WN;
+    const int gt = tp.full + t;
+    const int gm = (gt / tp.tiles_x) * C::BM + wm * 4 * TM + 4 * (lane >> 3) + 16 * (i / 4) + (i % 4);
+    const int64_t gn = (int64_t)(gt % tp.tiles_x) * C::BN + wn * 8 * TN + 4 * (lane & 7) + 32 * h;
+    if (gm >= M || gn >= N) return;
+    const int v0 = t * ktiles / tp.span, v1 = ((t + 1) * ktiles - 1) / tp.span;
+    const float4 *P = reinterpret_cast<const float4 *>(tp.partials);
+    float4 sum = __ldcg(P + (size_t)partial_slot(v0, t, tp.span, ktiles, tp.tail_iters) * PER_TILE + e);
+#pragma unroll 4
+    for (int w = v0 + 1; w <= v1; ++w) {
+        const float4 x = __ldcg(P + (size_t)partial_slot(w, t, tp.span, ktiles, tp.tail_iters) * PER_TILE + e);
+        sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
+    }
+    float v[4] = {ep.alpha * sum.x, ep.alpha * sum.y, ep.alpha * sum.z, ep.alpha * sum.w};
+    float *crow = Cm + (int64_t)gm * ldc;
+    const bool tail = ep.bias != nullptr || ep.act != kActNone;
+    if (c_vec4 && gn + 3 < N) {
+        float4 *p = reinterpret_cast<float4 *>(crow + gn);
+        if (ep.beta != 0.0f) {
+            const float4 o = *p;
+            v[0] = fmaf(ep.beta, o.x, v[0]);
+            v[1] = fmaf(ep.beta, o.y, v[1]);
+            v[2] = fmaf(ep.beta, o.z, v[2]);
+            v[3] = fmaf(ep.beta, o.w, v[3]);
+        }
+        if (tail) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = epilogue_tail(ep, v[k], gn + k);
+        }
+        *p = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (gn + k < N) {
+                float *p = crow + gn + k;
+                float w = (ep.beta != 0.0f) ? fmaf(ep.beta, *p, v[k]) : v[k];
+                if (tail) w = epilogue_tail(ep, w, gn + k);
+                *p = w;
+            }
+        }
+    }
 }
 
 // CTAs of the kernel one SM holds, per device (0 until asked).
@@ -480,6 +553,7 @@ struct Plan {
     int tiles_x = 0;
     int64_t tiles = 0, full = 0;
     int span = 0;              // 0: whole tiles only
+    bool reduce_pass = false;  // partial tiles summed by ffma_tail_reduce_kernel
     int64_t tail_units = 0;
     int64_t rem() const { return tiles - full; }
     int64_t units() const { return full + tail_units; }
@@ -511,6 +585,11 @@ Plan plan_units(const GemmArgs &g, int64_t at_floats, int64_t capacity) {
         if (span * C::BK + 2 * FFMA_SPLIT_C0 >= whole_cost) break;   // no cheaper than whole tiles
         q.span = (int)span;
         q.tail_units = (iters + span - 1) / span;
+        // The last unit to arrive at a tile would read the others' partial
+        // tiles one after another; a separate kernel sums every tile's
+        // partials at once, which measured as fast or faster on every shape.
+        const int forced = g_force_tail_sum.load(std::memory_order_relaxed);
+        q.reduce_pass = forced != 0;
         if (at_floats + partial_floats<C>(q) <= capacity) return q;   // the shortest span that fits
     }
     return p;
@@ -534,6 +613,7 @@ cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt, const Pl
     tp.tail_iters = (int)(p.rem() * ((g.K + C::BK - 1) / C::BK));
     tp.counters = reinterpret_cast<unsigned *>(extra);
     tp.partials = extra != nullptr ? extra + kCounterFloats : nullptr;
+    tp.reduce_pass = p.span > 0 && p.reduce_pass ? 1 : 0;
     const int c_vec4 = ((reinterpret_cast<uintptr_t>(g.C) & 15) == 0) && (g.ldc % 4 == 0);
     // a programmatic dependent of the transpose launched just before it
     cudaLaunchConfig_t cfg = {};
@@ -546,8 +626,16 @@ cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt, const Pl
     attr[0].val.programmaticStreamSerializationAllowed = FFMA_PDL;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ffma_tma_kernel<C>, tmAt, tmB, (int)g.M, (int)g.N, (int)g.K,
-                              g.epi(), g.C, g.ldc, c_vec4, tp, g.err, g.wait_ns);
+    e = cudaLaunchKernelEx(&cfg, ffma_tma_kernel<C>, tmAt, tmB, (int)g.M, (int)g.N, (int)g.K, g.epi(),
+                           g.C, g.ldc, c_vec4, tp, g.err, g.wait_ns);
+    if (e != cudaSuccess || !tp.reduce_pass) return e;
+    constexpr int per_tile = C::TM * C::TN / 4 * C::THREADS;
+    cudaLaunchConfig_t rcfg = cfg;
+    rcfg.gridDim = dim3((unsigned)((per_tile + 255) / 256), (unsigned)p.rem(), 1);
+    rcfg.blockDim = dim3(256, 1, 1);
+    rcfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&rcfg, ffma_tail_reduce_kernel<C>, tp, (int)((g.K + C::BK - 1) / C::BK),
+                              (int)g.M, (int)g.N, g.epi(), g.C, g.ldc, c_vec4);
 }
 
 }  // namespace
@@ -566,6 +654,23 @@ int ffma_config_for(int64_t M, int64_t N) {
 }
 
 int ffma_config_count() { return kFfmaConfigs; }
+
+void ffma_tma_plan_info(const GemmArgs &g, int64_t *units, int *span, int *tail_sum) {
+    const int64_t at = g.K * ffma_tma_at_ld(g.M);
+    with_config(ffma_config_for(g.M, g.N), [&](auto c) {
+        using C = decltype(c);
+        const Plan p = plan_units<C>(g, at, INT64_MAX);
+        *units = p.units();
+        *span = p.span;
+        *tail_sum = p.span > 0 && p.reduce_pass ? 1 : 0;
+        return 0;
+    });
+}
+
+int ffma_force_tail_sum(int mode) {
+    if (mode < -1 || mode > 1) return -2;
+    return g_force_tail_sum.exchange(mode);
+}
 
 int ffma_force_config(int idx) {
     if (idx < -1 || idx >= kFfmaConfigs) return -2;

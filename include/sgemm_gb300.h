@@ -388,12 +388,33 @@ int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
  *   sgemm_ffma_force_config   make every later FFMA-path call run configuration
  *                             `idx` (-1: back to the table); returns the
  *                             previous setting, or SGEMM_ERR_BAD_ARG
+ *   sgemm_ffma_force_tail_sum how later calls sum the partial tiles of a tail
+ *                             divided by work: -1 the library's default (a
+ *                             separate kernel over all tail tiles, launched
+ *                             after the tile kernel), 0 the last unit to
+ *                             reach each tile, inside the tile kernel, 1 the
+ *                             separate kernel.  Both add the partials in the
+ *                             same order, so results are the same bits.
+ *                             Returns the previous setting, or
+ *                             SGEMM_ERR_BAD_ARG for another value
+ *   sgemm_ffma_tail_plan      the work list an sgemm() call of this shape runs
+ *                             on the FFMA-TMA path on the current device:
+ *                             *units CTAs, *span k-tiles per unit of the
+ *                             divided tail (0: the tail is not divided) and
+ *                             *tail_sum 1 when a separate kernel sums the
+ *                             tail (the call then launches three kernels:
+ *                             transpose, tiles, sum), else 0.  Host only;
+ *                             SGEMM_OK, SGEMM_ERR_BAD_DIM for a dimension
+ *                             < 1, SGEMM_ERR_BAD_ARG for a NULL pointer, or
+ *                             SGEMM_ERR_DEVICE / SGEMM_ERR_CUDA
  */
 int sgemm_ffma_config_count(void);
 int sgemm_ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *threads,
                            int *ctas_per_sm);
 int sgemm_ffma_config_for(int64_t M, int64_t N);
 int sgemm_ffma_force_config(int idx);
+int sgemm_ffma_force_tail_sum(int mode);
+int sgemm_ffma_tail_plan(int64_t M, int64_t N, int64_t K, int64_t *units, int *span, int *tail_sum);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int sgemm_version(void);

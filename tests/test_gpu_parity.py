@@ -355,6 +355,48 @@ def test_every_ffma_config(cfg, M, N, K):
         sg.ffma_force_config(prev)
 
 
+# The partial tiles of a divided tail are summed either by a separate kernel
+# over all tail tiles at once (the default) or by the last unit to reach each
+# tile, inside the tile kernel.
+# Both add the same partials in the same order and apply the same epilogue,
+# so the two must agree bit for bit, and each must pass the oracle gate.
+# Covered: the 128x128 and 32x256 configurations, few and many partials per
+# tile, beta != 0, a fused bias + activation, and C rows that are not
+# 16-byte aligned (the scalar store path).
+TAIL_SUM_CASES = [
+    (1000, 1000, 1000, -1, 0.5, None, "none", 0),
+    (31, 3000, 2050, 4, 1.0, None, "none", 0),
+    (32, 1024, 4096, 4, -0.75, "bias", "silu", 0),
+    (300, 260, 516, 0, 1.25, None, "relu", 1),
+    (513, 384, 3000, 2, 0.0, "bias", "gelu", 1),
+]
+
+
+@pytest.mark.parametrize("M,N,K,cfg,beta,bias,act,ragged_c", TAIL_SUM_CASES)
+def test_tail_sum_by_kernel_matches_last_arriver(M, N, K, cfg, beta, bias, act, ragged_c):
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=M + N + K, beta=beta)
+    bvec = synth.matrix(1, N, seed=5, stream=3, dist="normal")[0] if bias else None
+    ldb = (N + 3) // 4 * 4
+    lds = (K, ldb, N + 1 if ragged_c else ldb)
+    prev_cfg = sg.ffma_force_config(cfg)
+    outs = []
+    try:
+        plan = sg.ffma_tail_plan(M, N, K)
+        assert plan["span"] > 0 and plan["tail_sum"] == 1, plan   # divided, summed by the kernel
+        for mode in (0, 1):
+            prev = sg.ffma_force_tail_sum(mode)
+            try:
+                _, chosen, C = run_checked(sg, A, B, C0, 1.5, beta, lds=lds, bias=bvec, act=act,
+                                           return_c=True)
+            finally:
+                sg.ffma_force_tail_sum(prev)
+            assert chosen == TMA
+            outs.append(C)
+    finally:
+        sg.ffma_force_config(prev_cfg)
+    assert np.array_equal(outs[0], outs[1]), "the two ways of summing the tail differ"
+
+
 # ---------------------------------------------------------------- fused epilogue
 # C = act(alpha*A@B + beta*C + bias[j]) on every kernel path: the TMA tile
 # kernel (whole tiles and a divided tail), the plain-load kernel, the
