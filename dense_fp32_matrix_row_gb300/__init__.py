@@ -81,7 +81,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_host_panel_rows.argtypes = [_i64, _i64, _i64]
         L.sgemm_host_panel_rows.restype = _i64
         L.sgemm_select_kernel.argtypes = _GEMM_ARGS[:-1] + [ctypes.c_int]
-        L.sgemm_ffma_config_for.argtypes = [_i64, _i64]
+        L.sgemm_ffma_config_for.argtypes = [_i64, _i64, _i64]
         L.sgemm_ffma_config_for.restype = ctypes.c_int
         L.sgemm_select_kernel.restype = ctypes.c_int
         L.sgemm_status.argtypes = [_vp]
@@ -280,9 +280,9 @@ def ffma_configs() -> list[dict]:
     return out
 
 
-def ffma_config_for(M: int, N: int) -> int:
+def ffma_config_for(M: int, N: int, K: int) -> int:
     """The tile configuration an FFMA-path call of this shape runs."""
-    return int(lib().sgemm_ffma_config_for(int(M), int(N)))
+    return int(lib().sgemm_ffma_config_for(int(M), int(N), int(K)))
 
 
 def ffma_force_config(idx: int) -> int:

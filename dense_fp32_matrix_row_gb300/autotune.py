@@ -86,7 +86,7 @@ def candidates(tiles=((8, 8),)) -> list[tuple[int, ...]]:
     out = []
     for (tm, tn), (wm, wn), bk, stages, minb in itertools.product(
             tiles, ((2, 2), (4, 2), (2, 4), (4, 1), (1, 4)),
-            (16, 32), (2, 3, 4), (1, 2, 4)):
+            (16, 32, 48), (2, 3, 4), (1, 2, 4)):
         warps = wm * wn * minb
         if wm * 4 * tm < 64 or wn * 8 * tn < 64 or not 8 <= warps <= 32:
             continue
@@ -98,19 +98,19 @@ def candidates(tiles=((8, 8),)) -> list[tuple[int, ...]]:
 def table_source(rows: list[tuple[int, int, int]], gpu: str, measured: dict,
                  exact: list[tuple[int, int, int, int]] = ()) -> str:
     """C++ source of the dispatch table: entries for the exact shapes (M, N, K,
-    config) first, then the classes (m_max, n_max, config) with -1 meaning
-    unbounded, in lookup order."""
+    config) first, then the classes (m_max, n_max, config; any K) with -1
+    meaning unbounded, in lookup order."""
     lim = lambda v: "INT64_MAX" if v < 0 else str(v)
-    body = "\n".join([f"    {{{M}, {M}, {N}, {N}, {c}}},   // {M}x{N}x{K}" for M, N, K, c in exact] +
-                     [f"    {{0, {lim(m)}, 0, {lim(n)}, {c}}}," for m, n, c in rows])
+    body = "\n".join([f"    {{{M}, {M}, {N}, {N}, {K}, {K}, {c}}},   // {M}x{N}x{K}" for M, N, K, c in exact] +
+                     [f"    {{0, {lim(m)}, 0, {lim(n)}, 0, INT64_MAX, {c}}}," for m, n, c in rows])
     exact_lines = "".join(f"//   {M}x{N}x{K} (exact): " + " ".join(f"{t:.1f}" for t in measured["exact"][f"{M}x{N}x{K}"])
                           + "\n" for M, N, K, _ in exact)
     return (
         "// ffma_tuning.inc -- which FFMA tile configuration runs each shape class.\n"
         "// Written by dense_fp32_matrix_row_gb300/autotune.py from measurements on\n"
         f"// {gpu}; rerun it (and rebuild) to retune.  Entries are tried in order; the\n"
-        "// first with m_lo <= M <= m_max and n_lo <= N <= n_max applies: the shapes\n"
-        "// measured exactly, then the classes.  A configuration other than the\n"
+        "// first with M, N and K inside its bounds applies: the shapes measured\n"
+        "// exactly (M, N and K), then the (M, N) classes.  A configuration other than the\n"
         f"// default wins only by {100 * (MARGIN - 1):.1f}% or more.\n"
         "// Configurations: " + "; ".join(
             f"{i} = {c['bm']}x{c['bn']} BK {c['bk']}, {c['stages']} stages, {c['ctas_per_sm']} CTAs/SM"
@@ -160,10 +160,8 @@ def run_table(out: str, exact_shapes=()) -> None:
     sg.build()
     configs = sg.ffma_configs()
     exact_tf, exact = {}, []
-    # the library looks entries up by (M, N): of exact shapes that share both,
-    # only the first gets an entry
     seen = set()
-    exact_shapes = [s for s in exact_shapes if not ((s[0], s[1]) in seen or seen.add((s[0], s[1])))]
+    exact_shapes = [s for s in exact_shapes if not (tuple(s) in seen or seen.add(tuple(s)))]
     for M, N, K in exact_shapes:
         tf = _measure(sg, torch, len(configs), [(M, N, K)])
         exact_tf[f"{M}x{N}x{K}"] = tf

@@ -461,7 +461,7 @@ int sgemm_ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int 
                                                                           : SGEMM_ERR_BAD_ARG;
 }
 
-int sgemm_ffma_config_for(int64_t M, int64_t N) { return ffma_config_for(M, N); }
+int sgemm_ffma_config_for(int64_t M, int64_t N, int64_t K) { return ffma_config_for(M, N, K); }
 
 int sgemm_ffma_force_config(int idx) {
     const int prev = ffma_force_config(idx);

@@ -71,7 +71,7 @@ int64_t ffma_tma_workspace_floats(const GemmArgs &g, int64_t capacity);
 // Tile configurations of the FFMA kernel: the one a shape runs (the tuning
 // table, or the forced one), their number, forcing one (-1: the table;
 // returns the previous setting, -2 for a bad index), and their parameters.
-int ffma_config_for(int64_t M, int64_t N);
+int ffma_config_for(int64_t M, int64_t N, int64_t K);
 int ffma_config_count();
 int ffma_force_config(int idx);
 int ffma_force_tail_sum(int mode);   // -1 default, 0 last arriver, 1 separate kernel; -2 if invalid

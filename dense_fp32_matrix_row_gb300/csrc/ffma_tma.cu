@@ -68,7 +68,7 @@
 #define FFMA_STAGES 2
 #endif
 #ifndef FFMA_BK
-#define FFMA_BK 32
+#define FFMA_BK 48   // k-steps per k-tile of the default configuration
 #endif
 #ifndef FFMA_MINB
 #define FFMA_MINB 2
@@ -108,12 +108,13 @@ struct Cfg {
 // The tile configurations compiled into the library (the search space of the
 // tuning script, dense_fp32_matrix_row_gb300/autotune.py).  Index 0 is the
 // default; ffma_tuning.inc maps shape classes to an index.
-using Default = Cfg<FFMA_TM, FFMA_TN, FFMA_WM, FFMA_WN, FFMA_BK, FFMA_STAGES, FFMA_MINB>;   // 128 x 128
+using Default = Cfg<FFMA_TM, FFMA_TN, FFMA_WM, FFMA_WN, FFMA_BK, FFMA_STAGES, FFMA_MINB>;   // 128 x 128, BK 48
 using Wide = Cfg<8, 8, 2, 4, 32, 2, 2>;                                         // 64 x 256
 using Narrow = Cfg<8, 8, 4, 1, 32, 2, 4>;                                       // 128 x 64
 using ShallowK = Cfg<8, 8, 4, 2, 16, 4, 2>;                                     // 128 x 128, BK 16
 using Skinny = Cfg<8, 8, 1, 4, FFMA_SK_BK, FFMA_SK_STAGES, FFMA_SK_MINB>;          // 32 x 256
-constexpr int kFfmaConfigs = 5;
+using Base32 = Cfg<8, 8, 4, 2, 32, 2, 2>;                                       // 128 x 128, BK 32
+constexpr int kFfmaConfigs = 6;
 
 // f(C{}) for the configuration with index `idx`.
 template <class F>
@@ -123,12 +124,13 @@ decltype(auto) with_config(int idx, F &&f) {
         case 2: return f(Narrow{});
         case 3: return f(ShallowK{});
         case 4: return f(Skinny{});
+        case 5: return f(Base32{});
         default: return f(Default{});
     }
 }
 
 struct FfmaTuneEntry {
-    int64_t m_lo, m_max, n_lo, n_max;   // applies to m_lo <= M <= m_max, n_lo <= N <= n_max
+    int64_t m_lo, m_max, n_lo, n_max, k_lo, k_max;   // applies inside these bounds on M, N, K
     int config;
 };
 #include "ffma_tuning.inc"
@@ -644,11 +646,11 @@ int64_t ffma_tma_max_m() { return (int64_t)65535 * Default::BM; }
 
 int64_t ffma_tma_at_ld(int64_t M) { return (M + 3) / 4 * 4; }
 
-int ffma_config_for(int64_t M, int64_t N) {
+int ffma_config_for(int64_t M, int64_t N, int64_t K) {
     const int forced = g_force_config.load(std::memory_order_relaxed);
     if (forced >= 0 && forced < kFfmaConfigs) return forced;
     for (const FfmaTuneEntry &e : kFfmaTune)
-        if (e.m_lo <= M && M <= e.m_max && e.n_lo <= N && N <= e.n_max)
+        if (e.m_lo <= M && M <= e.m_max && e.n_lo <= N && N <= e.n_max && e.k_lo <= K && K <= e.k_max)
             return (e.config >= 0 && e.config < kFfmaConfigs) ? e.config : 0;
     return 0;
 }
@@ -657,7 +659,7 @@ int ffma_config_count() { return kFfmaConfigs; }
 
 void ffma_tma_plan_info(const GemmArgs &g, int64_t *units, int *span, int *tail_sum) {
     const int64_t at = g.K * ffma_tma_at_ld(g.M);
-    with_config(ffma_config_for(g.M, g.N), [&](auto c) {
+    with_config(ffma_config_for(g.M, g.N, g.K), [&](auto c) {
         using C = decltype(c);
         const Plan p = plan_units<C>(g, at, INT64_MAX);
         *units = p.units();
@@ -690,7 +692,7 @@ bool ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *thre
 
 int64_t ffma_tma_workspace_floats(const GemmArgs &g, int64_t capacity) {
     const int64_t at = g.K * ffma_tma_at_ld(g.M);
-    return with_config(ffma_config_for(g.M, g.N), [&](auto c) -> int64_t {
+    return with_config(ffma_config_for(g.M, g.N, g.K), [&](auto c) -> int64_t {
         using C = decltype(c);
         return at + partial_floats<C>(plan_units<C>(g, at, capacity));
     });
@@ -699,7 +701,7 @@ int64_t ffma_tma_workspace_floats(const GemmArgs &g, int64_t capacity) {
 cudaError_t launch_ffma_tma(const GemmArgs &g, float *workspace, int64_t capacity) {
     const int64_t ldt = ffma_tma_at_ld(g.M);
     const int64_t at = g.K * ldt;
-    return with_config(ffma_config_for(g.M, g.N), [&](auto c) -> cudaError_t {
+    return with_config(ffma_config_for(g.M, g.N, g.K), [&](auto c) -> cudaError_t {
         using C = decltype(c);
         const Plan p = plan_units<C>(g, at, capacity);
         float *extra = p.span > 0 ? workspace + at : nullptr;

@@ -375,7 +375,8 @@ int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
  * 接近 cuBLAS", section "8. Kernel 9: 参数自动调优", done per shape class).  The
  * library holds several compile-time tile configurations of the FFMA kernel;
  * a table written by dense_fp32_matrix_row_gb300/autotune.py from
- * measurements picks one per (M, N) class.  These calls serve that script and
+ * measurements picks one per shape measured exactly (M, N and K) and per
+ * (M, N) class otherwise.  These calls serve that script and
  * the tests; they do not change results beyond rounding order.
  *   sgemm_ffma_config_count   number of configurations (indices 0 .. n-1;
  *                             0 is the default)
@@ -383,8 +384,8 @@ int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
  *                             stages, threads per CTA, CTAs per SM the
  *                             registers are sized for; 0, or SGEMM_ERR_BAD_ARG
  *                             for an unknown index or a NULL pointer
- *   sgemm_ffma_config_for     the configuration an FFMA-path call of this M, N
- *                             runs (host only)
+ *   sgemm_ffma_config_for     the configuration an FFMA-path call of this M, N,
+ *                             K runs (host only)
  *   sgemm_ffma_force_config   make every later FFMA-path call run configuration
  *                             `idx` (-1: back to the table); returns the
  *                             previous setting, or SGEMM_ERR_BAD_ARG
@@ -411,7 +412,7 @@ int sgemm_noalloc(int64_t M, int64_t N, int64_t K, float alpha,
 int sgemm_ffma_config_count(void);
 int sgemm_ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *threads,
                            int *ctas_per_sm);
-int sgemm_ffma_config_for(int64_t M, int64_t N);
+int sgemm_ffma_config_for(int64_t M, int64_t N, int64_t K);
 int sgemm_ffma_force_config(int idx);
 int sgemm_ffma_force_tail_sum(int mode);
 int sgemm_ffma_tail_plan(int64_t M, int64_t N, int64_t K, int64_t *units, int *span, int *tail_sum);

@@ -14,8 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 TABLE = os.path.join(ROOT, "dense_fp32_matrix_row_gb300", "csrc", "ffma_tuning.inc")
 
 # (TM, TN, WM, WN, BK, STAGES, MINB) of the configurations compiled into the library
-COMPILED = [(8, 8, 4, 2, 32, 2, 2), (8, 8, 2, 4, 32, 2, 2), (8, 8, 4, 1, 32, 2, 4),
-            (8, 8, 4, 2, 16, 4, 2), (8, 8, 1, 4, 32, 2, 3)]
+COMPILED = [(8, 8, 4, 2, 48, 2, 2), (8, 8, 2, 4, 32, 2, 2), (8, 8, 4, 1, 32, 2, 4),
+            (8, 8, 4, 2, 16, 4, 2), (8, 8, 1, 4, 32, 2, 3), (8, 8, 4, 2, 32, 2, 2)]
 
 
 @pytest.fixture(scope="module")
@@ -47,7 +47,7 @@ def test_illegal_configurations_are_rejected(cfg, why):
 
 def test_search_space():
     c = autotune.candidates()
-    assert (8, 8, 4, 2, 32, 2, 2) in c                # the default is searched
+    assert (8, 8, 4, 2, 48, 2, 2) in c                # the default is searched
     assert all(autotune.legal(*x)[0] for x in c)
     assert all(8 <= x[2] * x[3] * x[6] <= 32 for x in c)
     assert len(autotune.candidates(((8, 8), (8, 4), (4, 8)))) > len(c)
@@ -56,7 +56,7 @@ def test_search_space():
 def _compile_table(tmp_path, text):
     src = tmp_path / "t.cc"
     src.write_text("#include <cstdint>\n#include <cstdio>\n"
-                   "struct FfmaTuneEntry { int64_t m_lo, m_max, n_lo, n_max; int config; };\n" + text +
+                   "struct FfmaTuneEntry { int64_t m_lo, m_max, n_lo, n_max, k_lo, k_max; int config; };\n" + text +
                    "int main() { std::printf(\"%d\\n\", (int)(sizeof(kFfmaTune) / sizeof(kFfmaTune[0]))); }\n")
     exe = tmp_path / "t"
     subprocess.run(["g++", "-std=c++17", "-Wall", "-Werror", str(src), "-o", str(exe)], check=True)
@@ -64,12 +64,17 @@ def _compile_table(tmp_path, text):
 
 
 def _entries(text):
-    """(m_lo, m_max, n_lo, n_max, config) of every table entry."""
+    """(m_lo, m_max, n_lo, n_max, k_lo, k_max, config) of every table entry."""
     v = r"(INT64_MAX|\d+)"
-    rows = re.findall(r"\{\s*" + r",\s*".join([v] * 4) + r",\s*(\d+)\s*\}", text)
+    rows = re.findall(r"\{\s*" + r",\s*".join([v] * 6) + r",\s*(\d+)\s*\}", text)
     big = 2 ** 63 - 1
     num = lambda x: big if x == "INT64_MAX" else int(x)
-    return [tuple(num(x) for x in r[:4]) + (int(r[4]),) for r in rows]
+    return [tuple(num(x) for x in r[:6]) + (int(r[6]),) for r in rows]
+
+
+def _lookup(entries, M, N, K):
+    return next(e[6] for e in entries
+                if e[0] <= M <= e[1] and e[2] <= N <= e[3] and e[4] <= K <= e[5])
 
 
 def test_generated_table_compiles(tmp_path):
@@ -80,8 +85,8 @@ def test_generated_table_compiles(tmp_path):
     text = autotune.table_source(rows, "test GPU", measured, [(4092, 4092, 4092, 1)])
     assert _compile_table(tmp_path, text) == 4
     big = 2 ** 63 - 1
-    assert _entries(text) == [(4092, 4092, 4092, 4092, 1), (0, 64, 0, 256, 1), (0, 64, 0, big, 0),
-                              (0, big, 0, big, 0)]
+    assert _entries(text) == [(4092, 4092, 4092, 4092, 4092, 4092, 1), (0, 64, 0, 256, 0, big, 1),
+                              (0, 64, 0, big, 0, big, 0), (0, big, 0, big, 0, big, 0)]
 
 
 def test_committed_table(tmp_path, L):
@@ -90,13 +95,17 @@ def test_committed_table(tmp_path, L):
     entries = _entries(text)
     assert len(entries) == n and n >= 1
     big = 2 ** 63 - 1
-    assert entries[-1][:4] == (0, big, 0, big), "the last entry must catch every shape"
-    assert all(0 <= e[4] < len(COMPILED) for e in entries)
+    assert entries[-1][:6] == (0, big, 0, big, 0, big), "the last entry must catch every shape"
+    assert all(0 <= e[6] < len(COMPILED) for e in entries)
     # the library's lookup is the first matching entry
     for M in (17, 64, 65, 128, 300, 1024, 4092, 8192, 9000):
         for N in (8, 256, 257, 1024, 4092, 12288, 14336):
-            want = next(e[4] for e in entries if e[0] <= M <= e[1] and e[2] <= N <= e[3])
-            assert sg.ffma_config_for(M, N) == want, (M, N)
+            for K in (64, 1024, 4092, 4096, 8192):
+                assert sg.ffma_config_for(M, N, K) == _lookup(entries, M, N, K), (M, N, K)
+    # exact shapes match on K too
+    for e in entries:
+        if e[0] == e[1] and e[4] == e[5]:
+            assert sg.ffma_config_for(e[0], e[2], e[4]) == e[6]
 
 
 def test_forcing_a_configuration(L):
@@ -104,11 +113,10 @@ def test_forcing_a_configuration(L):
     prev = sg.ffma_force_config(2)
     try:
         assert prev == -1
-        assert sg.ffma_config_for(4092, 4092) == 2
+        assert sg.ffma_config_for(4092, 4092, 4092) == 2
     finally:
         sg.ffma_force_config(-1)
-    assert sg.ffma_config_for(4092, 4092) == next(
-        e[4] for e in _entries(open(TABLE).read()) if e[0] <= 4092 <= e[1] and e[2] <= 4092 <= e[3])
+    assert sg.ffma_config_for(4092, 4092, 4092) == _lookup(_entries(open(TABLE).read()), 4092, 4092, 4092)
 
 
 def test_pick_keeps_the_default_within_the_margin():

@@ -338,11 +338,11 @@ def test_pair_tiles(mode, M, N, K):
 # ---------------------------------------------------------------- FFMA tile configurations
 # Every configuration compiled into the library (the autotuner's choices),
 # forced, on shapes with ragged edges, a divided tail and beta != 0.
-@pytest.mark.parametrize("cfg", range(5))
+@pytest.mark.parametrize("cfg", range(6))
 @pytest.mark.parametrize("M,N,K", [(300, 260, 516), (1500, 1100, 700), (129, 1000, 77),
                                    (2300, 2352, 1001), (31, 3000, 2050)])
 def test_every_ffma_config(cfg, M, N, K):
-    assert len(sg.ffma_configs()) == 5
+    assert len(sg.ffma_configs()) == 6
     A, B, C0 = make_inputs(M, N, K, "normal", seed=M + cfg, beta=0.5)
     ldb = (N + 3) // 4 * 4
     prev = sg.ffma_force_config(cfg)
