@@ -241,14 +241,14 @@ __device__ __forceinline__ void store_tile(const float (&acc)[C::TM][C::TN], int
 // whatever the tile count (the "stream-K" division).  A unit's run may end
 // part of one tile and start the next.  For each tile it touches without
 // covering it whole, the unit writes its partial tile to a slot of
-// `partials` and counts the tile's arrival in counters[tile - full] (zeroed
-// before the launch); the unit that completes the count sums the tile's
-// partial tiles in unit order and runs the epilogue.  No unit waits for
-// another, and the sum order does not depend on timing.  By default the
-// units only write their partial tiles and ffma_tail_reduce_kernel, launched
-// right after the tile kernel, sums every tile's partials in the same order
-// (reduce_pass); the in-kernel sum by the last unit to arrive remains
-// selectable (sgemm_ffma_force_tail_sum) and gives the same bits.
+// `partials`.  By default (reduce_pass) that is all: ffma_tail_reduce_kernel,
+// launched right after the tile kernel, sums every tail tile's partial tiles
+// in unit order and runs the epilogue.  The alternative, selectable with
+// sgemm_ffma_force_tail_sum and giving the same bits, sums inside this
+// kernel: each unit counts the tile's arrival in counters[tile - full]
+// (zeroed before the launch) and the unit that completes the count sums the
+// tile's partial tiles in unit order.  No unit waits for another, and the
+// sum order does not depend on timing.
 struct TailPlan {
     int tiles_x;
     int full;             // whole-tile units
