@@ -16,7 +16,7 @@ import os
 from .build import LIBRARY, build  # noqa: F401  (build is part of the public API)
 
 __all__ = ["sgemm", "sgemm_host", "host_set_panels", "host_panel_rows", "sgemm_3xtf32", "sgemm_tf32", "sgemm_bf16", "sgemm_ptr", "status", "select_kernel",
-           "force_kernel", "ffma_configs", "ffma_config_for", "ffma_force_config", "ffma_force_tail_sum", "ffma_tail_plan", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
+           "force_kernel", "ffma_configs", "ffma_config_for", "ffma_force_config", "ffma_force_tail_sum", "ffma_tail_plan", "kernel_timing", "kernel_timing_result", "set_wait_limit", "selftest_wait", "release_workspaces", "status_string",
            "version", "SgemmError", "lib"]
 
 OK = 0
@@ -308,6 +308,26 @@ def ffma_tail_plan(M: int, N: int, K: int) -> dict:
     if rc != OK:
         raise SgemmError(rc, "sgemm_ffma_tail_plan")
     return {"units": units.value, "span": span.value, "tail_sum": ts.value}
+
+
+def kernel_timing(enable: bool) -> int:
+    """Start (clearing earlier records) or stop bracketing each FFMA tile
+    kernel with CUDA events; returns the previous state."""
+    rc = int(lib().sgemm_kernel_timing(1 if enable else 0))
+    if rc < 0:
+        raise SgemmError(rc, "sgemm_kernel_timing")
+    return rc
+
+
+def kernel_timing_result() -> tuple[float, int]:
+    """(summed ms, launches) of the FFMA tile kernels recorded since timing started."""
+    ms, n = ctypes.c_double(), ctypes.c_int64()
+    f = lib().sgemm_kernel_timing_result
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    rc = f(ctypes.addressof(ms), ctypes.addressof(n))
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_kernel_timing_result")
+    return ms.value, n.value
 
 
 def set_wait_limit(ns: int) -> int:

@@ -487,6 +487,16 @@ int sgemm_ffma_tail_plan(int64_t M, int64_t N, int64_t K, int64_t *units, int *s
     return SGEMM_OK;
 }
 
+int sgemm_kernel_timing(int enable) {
+    const int prev = kernel_timing(enable);
+    return prev == -2 ? SGEMM_ERR_BAD_ARG : prev;
+}
+
+int sgemm_kernel_timing_result(double *total_ms, int64_t *launches) {
+    if (!total_ms || !launches) return SGEMM_ERR_BAD_ARG;
+    return kernel_timing_result(total_ms, launches) ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
 int sgemm_version(void) { return 100; }
 
 }  // extern "C"

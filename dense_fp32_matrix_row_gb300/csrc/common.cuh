@@ -79,6 +79,11 @@ int ffma_force_tail_sum(int mode);   // -1 default, 0 last arriver, 1 separate k
 // units (CTAs), span (k-tiles per tail unit, 0 when the tail is not
 // divided) and whether a separate kernel sums the tail (1) or not (0).
 void ffma_tma_plan_info(const GemmArgs &g, int64_t *units, int *span, int *tail_sum);
+// sgemm_kernel_timing: start (1, clearing earlier records) or stop (0) the
+// event pairs around FFMA tile-kernel launches; -2 for another value.
+int kernel_timing(int enable);
+// Summed elapsed time of the recorded tile kernels (waits for them).
+bool kernel_timing_result(double *total_ms, int64_t *launches);
 bool ffma_config_info(int idx, int *bm, int *bn, int *bk, int *stages, int *threads, int *minb);
 int64_t ffma_tma_at_ld(int64_t M);
 // Largest M the TMA FFMA kernel's grid can cover.

@@ -40,6 +40,7 @@
 //                                 and columns wn*8*TN + 32*(j/4) + 4*tx + j%4   (j < TN).
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -137,6 +138,42 @@ struct FfmaTuneEntry {
 
 std::atomic<int> g_force_config{-1};
 std::atomic<int> g_force_tail_sum{-1};   // sgemm_ffma_force_tail_sum
+
+// sgemm_kernel_timing: event pairs around the tile-kernel launches.
+constexpr int kTimingSlots = 4096;
+std::mutex g_timing_mu;
+std::atomic<int> g_timing_on{0};
+int g_timing_used = 0;
+cudaEvent_t g_timing_ev[kTimingSlots][2] = {};
+int g_timing_dev[kTimingSlots] = {};
+
+// The event pair for the next launch (created on first use), or false when
+// recording is off or every slot is taken.
+bool timing_slot(cudaEvent_t &e0, cudaEvent_t &e1) {
+    if (!g_timing_on.load(std::memory_order_relaxed)) return false;
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    if (g_timing_used >= kTimingSlots) return false;
+    const int i = g_timing_used;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    for (int k = 0; k < 2; ++k) {
+        // events belong to the device that was current when they were made
+        if (g_timing_ev[i][k] != nullptr && g_timing_dev[i] != dev) {
+            (void)cudaEventDestroy(g_timing_ev[i][k]);
+            g_timing_ev[i][k] = nullptr;
+        }
+        if (g_timing_ev[i][k] == nullptr && cudaEventCreate(&g_timing_ev[i][k]) != cudaSuccess) {
+            (void)cudaGetLastError();
+            g_timing_ev[i][k] = nullptr;
+            return false;
+        }
+    }
+    g_timing_dev[i] = dev;
+    e0 = g_timing_ev[i][0];
+    e1 = g_timing_ev[i][1];
+    ++g_timing_used;
+    return true;
+}
 
 __device__ __forceinline__ float comp(const float4 &v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -628,8 +665,12 @@ cudaError_t launch_cfg(const GemmArgs &g, const float *At, int64_t ldt, const Pl
     attr[0].val.programmaticStreamSerializationAllowed = FFMA_PDL;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cudaEvent_t t0 = nullptr, t1 = nullptr;
+    const bool timed = timing_slot(t0, t1);
+    if (timed && (e = cudaEventRecord(t0, g.stream)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, ffma_tma_kernel<C>, tmAt, tmB, (int)g.M, (int)g.N, (int)g.K, g.epi(),
                            g.C, g.ldc, c_vec4, tp, g.err, g.wait_ns);
+    if (e == cudaSuccess && timed) e = cudaEventRecord(t1, g.stream);
     if (e != cudaSuccess || !tp.reduce_pass) return e;
     constexpr int per_tile = C::TM * C::TN / 4 * C::THREADS;
     cudaLaunchConfig_t rcfg = cfg;
@@ -667,6 +708,36 @@ void ffma_tma_plan_info(const GemmArgs &g, int64_t *units, int *span, int *tail_
         *tail_sum = p.span > 0 && p.reduce_pass ? 1 : 0;
         return 0;
     });
+}
+
+int kernel_timing(int enable) {
+    if (enable != 0 && enable != 1) return -2;
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    if (enable) g_timing_used = 0;
+    return g_timing_on.exchange(enable);
+}
+
+bool kernel_timing_result(double *total_ms, int64_t *launches) {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    double sum = 0.0;
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return false;
+    bool ok = true;
+    for (int i = 0; i < g_timing_used && ok; ++i) {
+        float ms = 0.0f;
+        ok = cudaSetDevice(g_timing_dev[i]) == cudaSuccess &&
+             cudaEventSynchronize(g_timing_ev[i][1]) == cudaSuccess &&
+             cudaEventElapsedTime(&ms, g_timing_ev[i][0], g_timing_ev[i][1]) == cudaSuccess;
+        sum += ms;
+    }
+    if (cudaSetDevice(cur) != cudaSuccess) ok = false;
+    if (!ok) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    *total_ms = sum;
+    *launches = g_timing_used;
+    return true;
 }
 
 int ffma_force_tail_sum(int mode) {

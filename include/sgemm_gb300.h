@@ -417,6 +417,30 @@ int sgemm_ffma_force_config(int idx);
 int sgemm_ffma_force_tail_sum(int mode);
 int sgemm_ffma_tail_plan(int64_t M, int64_t N, int64_t K, int64_t *units, int *span, int *tail_sum);
 
+/*
+ * Kernel timing, a measurement hook (the benchmark's roofline figure uses it
+ * to time the FFMA tile kernel apart from the transpose before it and the
+ * tail sum after it).
+ *   sgemm_kernel_timing(1)        start: every later FFMA-path call brackets
+ *                                 its tile kernel with two CUDA events on its
+ *                                 stream (up to 4096 launches are recorded;
+ *                                 later ones are not); clears earlier records
+ *   sgemm_kernel_timing(0)        stop recording
+ *                                 Both return the previous state (0 or 1), or
+ *                                 SGEMM_ERR_BAD_ARG for another value.
+ *   sgemm_kernel_timing_result    waits for the recorded events and returns
+ *                                 the tile kernels' summed time in *total_ms
+ *                                 and their number in *launches; SGEMM_OK,
+ *                                 SGEMM_ERR_BAD_ARG for a NULL pointer, or
+ *                                 SGEMM_ERR_CUDA
+ * The events sit between the transpose and the tile kernel on the stream, so
+ * while recording the tile kernel does not start its set-up during the
+ * transpose's tail; results are unchanged.  Not for use during stream
+ * capture (the events would be captured).
+ */
+int sgemm_kernel_timing(int enable);
+int sgemm_kernel_timing_result(double *total_ms, int64_t *launches);
+
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 int sgemm_version(void);
 

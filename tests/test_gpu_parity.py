@@ -659,3 +659,38 @@ def test_large_small_integers_exact():
     A, B, C0 = make_inputs(2200, 2400, 300, "int", seed=9, beta=-1.0)
     _, chosen = run_checked(sg, A, B, C0, 2.0, -1.0, exact=True)
     assert chosen == TMA
+
+
+def test_kernel_timing_hook():
+    # the events bracket the tile kernel only: its time is below the calls'
+    # time, one record per FFMA-path call, none for the decode path
+    import oracle
+    from gpu_util import normwise_err
+    M = N = K = 1024
+    A, B, C0 = make_inputs(M, N, K, "normal", seed=5)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    dC = torch.empty((M, N), device="cuda")
+    dA16 = dA[:16].contiguous()
+    dC16 = torch.empty((16, N), device="cuda")
+    assert sg.lib().sgemm_kernel_timing(2) == sg.ERR_BAD_ARG
+    assert sg.kernel_timing(True) == 0
+    try:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            sg.sgemm(dA, dB, dC)
+            sg.sgemm(dA16, dB, dC16)
+        e1.record()
+        torch.cuda.synchronize()
+    finally:
+        assert sg.kernel_timing(False) == 1
+    total, n = sg.kernel_timing_result()
+    assert n == 3
+    assert 0.0 < total < e0.elapsed_time(e1)
+    assert sg.status() == sg.OK
+    ref = oracle.sgemm(A, B, alpha=1.0, beta=0.0)
+    assert normwise_err(dC.cpu().numpy(), ref, A, B, K) <= GATE
+    # stopped: later calls add nothing
+    sg.sgemm(dA, dB, dC)
+    torch.cuda.synchronize()
+    assert sg.kernel_timing_result()[1] == 3
