@@ -276,6 +276,38 @@ def timed_steps(fn, steps, stream):
     return total, per
 
 
+def roofline_for(kid, M, N, K, beta, per_launch_ms, kernel_ms, sms, peaks):
+    """(bound, achieved, peak, unit, peak_source) of the main line: the FFMA
+    path against the FP32 FFMA peak (the tile kernel's own time when
+    kernel_ms is given, else the whole call), the tensor-core paths against
+    the tensor peak of their operand type (3xTF32 counts its three TF32
+    products), the decode path against the measured copy bandwidth."""
+    import dense_fp32_matrix_row_gb300 as sg
+    from dense_fp32_matrix_row_gb300 import accounting as acc
+    flops = acc.gemm_flops(M, N, K)
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    peak = acc.ffma_peak_tflops(sms, mhz)
+    achieved = flops / ((kernel_ms or per_launch_ms) * 1e-3) / 1e12
+    bound, unit = "alu", "TFLOP/s"
+    peak_source = (f"{sms} SMs x 128 FP32 lanes x 2 FLOP x {mhz:.0f} MHz "
+                   f"({peaks.get('_source', 'measured')} max clock)")
+    if kid in (sg.KERNEL_TF32X3, sg.KERNEL_TF32, sg.KERNEL_BF16):
+        bound = "tensor"
+        if kid == sg.KERNEL_BF16:
+            peak, peak_source = peaks["bf16_tflops"], "measured bf16 GEMM burst"
+        else:
+            peak = acc.tf32_peak_from_bf16(peaks["bf16_tflops"])
+            peak_source = "measured bf16 GEMM burst x 1.1/2.25 (nominal TF32/BF16 ratio)"
+        if kid == sg.KERNEL_TF32X3:
+            achieved *= 3      # three TF32 products per useful product
+    if kid == sg.KERNEL_DECODE:
+        # M <= 16: bound by streaming B, measured against the copy bandwidth
+        bound, unit = "hbm", "GB/s"
+        achieved = acc.min_traffic_bytes(M, N, K, beta != 0.0) / (per_launch_ms * 1e-3) / 1e9
+        peak, peak_source = peaks["hbm_gbs"], "measured HBM copy bandwidth"
+    return bound, achieved, peak, unit, peak_source
+
+
 def gate_err(got, ref, A, B, K, alpha, beta, C0, bias=None):
     """The acceptance gate as a number (<= 1e-6 passes): per element,
     |C - C_ref| against 1e-6*|alpha|*K*max|A|*max|B| plus, where beta != 0
@@ -689,26 +721,8 @@ def run_ours(args, world, rank, local):
         return 0
 
     props = torch.cuda.get_device_properties(dev)
-    peak = acc.ffma_peak_tflops(props.multi_processor_count, float(peaks.get("sm_max_mhz", 2070.0)))
-    achieved = flops / ((kernel_ms or per_launch_ms) * 1e-3) / 1e12
-    bound, peak_source = "alu", (f"{props.multi_processor_count} SMs x 128 FP32 lanes x 2 FLOP x "
-                                 f"{peaks.get('sm_max_mhz', 2070.0):.0f} MHz ({peaks['_source']} max clock)")
-    if kid in (sg.KERNEL_TF32X3, sg.KERNEL_TF32, sg.KERNEL_BF16):
-        # tensor work against the tensor peak of the operand type
-        bound = "tensor"
-        if kid == sg.KERNEL_BF16:
-            peak, peak_source = peaks["bf16_tflops"], "measured bf16 GEMM burst"
-        else:
-            peak = acc.tf32_peak_from_bf16(peaks["bf16_tflops"])
-            peak_source = "measured bf16 GEMM burst x 1.1/2.25 (nominal TF32/BF16 ratio)"
-        if kid == sg.KERNEL_TF32X3:
-            achieved *= 3      # three TF32 products per useful product
-    unit = "TFLOP/s"
-    if kid == sg.KERNEL_DECODE:
-        # M <= 16: bound by streaming B, measured against the copy bandwidth
-        bound, unit = "hbm", "GB/s"
-        achieved = acc.min_traffic_bytes(M, N, K, beta != 0.0) / (per_launch_ms * 1e-3) / 1e9
-        peak, peak_source = peaks["hbm_gbs"], "measured HBM copy bandwidth"
+    bound, achieved, peak, unit, peak_source = roofline_for(
+        kid, M, N, K, beta, per_launch_ms, kernel_ms, props.multi_processor_count, peaks)
     traffic = ncu_traffic("ffma_tma", name) if kid == sg.KERNEL_FFMA_TMA else None
     cpu = None
     if not args.no_cpu_baseline:

@@ -70,3 +70,35 @@ def test_source_hash_ignores_comments_only():
     assert bench._code_only(code) == bench._code_only(same)
     assert bench._code_only(code) != bench._code_only(other)
     assert bench._code_only(code) != bench._code_only(strings)
+
+
+PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "sm_max_mhz": 2000.0, "_source": "measured"}
+
+
+def test_roofline_ffma_uses_the_tile_kernel_time_when_given():
+    import dense_fp32_matrix_row_gb300 as sg
+    M = N = K = 1000
+    flops = 2 * M * N * K
+    b, ach, peak, unit, _ = bench.roofline_for(sg.KERNEL_FFMA_TMA, M, N, K, 0.5, 0.2, 0.1, 100, PEAKS)
+    assert (b, unit) == ("alu", "TFLOP/s")
+    assert peak == pytest.approx(100 * 128 * 2 * 2000e6 / 1e12)
+    assert ach == pytest.approx(flops / 0.1e-3 / 1e12)              # the kernel's own 0.1 ms
+    _, ach2, _, _, _ = bench.roofline_for(sg.KERNEL_FFMA_TMA, M, N, K, 0.5, 0.2, None, 100, PEAKS)
+    assert ach2 == pytest.approx(flops / 0.2e-3 / 1e12)             # else the whole call
+
+
+def test_roofline_tensor_and_decode_bounds():
+    import dense_fp32_matrix_row_gb300 as sg
+    M = N = K = 1000
+    flops = 2 * M * N * K
+    b, ach, peak, _, _ = bench.roofline_for(sg.KERNEL_TF32X3, M, N, K, 0.0, 0.1, None, 100, PEAKS)
+    assert b == "tensor" and ach == pytest.approx(3 * flops / 0.1e-3 / 1e12)
+    assert peak == pytest.approx(1900.0 * 1.1 / 2.25)
+    b, ach, peak, _, _ = bench.roofline_for(sg.KERNEL_BF16, M, N, K, 0.0, 0.1, None, 100, PEAKS)
+    assert b == "tensor" and ach == pytest.approx(flops / 0.1e-3 / 1e12) and peak == 1900.0
+    # decode: bytes of A, B and C (read too when beta != 0) against the copy bandwidth
+    b, ach, peak, unit, _ = bench.roofline_for(sg.KERNEL_DECODE, 16, 14336, 4096, 1.0, 0.05, None, 100,
+                                              PEAKS)
+    assert (b, unit, peak) == ("hbm", "GB/s", 6800.0)
+    nbytes = 4 * (16 * 4096 + 4096 * 14336 + 2 * 16 * 14336)
+    assert ach == pytest.approx(nbytes / 0.05e-3 / 1e9)
